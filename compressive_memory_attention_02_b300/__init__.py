@@ -1,0 +1,189 @@
+"""Python binding of liblinattn.so: causal linear attention (phi = elu + 1) on B300.
+
+Argument marshalling only. Every function has the name and argument order of
+the C entry point it wraps (include/linattn.h); tensors are passed as torch
+tensors (their device pointers are taken) or as raw integer addresses, None is
+NULL, and `stream` defaults to torch's current stream on the tensors' device.
+Every step of the computation runs in the library's CUDA kernels; there is no
+other implementation here, and importing fails loudly if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblinattn.so")
+
+LA_F32, LA_BF16 = 0, 1
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
+
+EXPORTS = (
+    "la_causal_fwd", "la_causal_fwd_ex", "la_causal_fwd_workspace_size",
+    "la_prefill_state", "la_prefill_state_ex", "la_prefill_workspace_size",
+    "la_decode_step", "la_set_workspace", "la_get_last_device_status",
+    "la_get_error_string", "la_last_launch_count",
+)
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {code} ({error_string(code)})")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m compressive_memory_attention_02_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    fwd = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, f32, i32]
+    lib.la_causal_fwd.argtypes = fwd + [vp]
+    lib.la_causal_fwd_ex.argtypes = fwd + [i64p, vp, sz, vp]
+    lib.la_causal_fwd_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32]
+    lib.la_causal_fwd_workspace_size.restype = sz
+    lib.la_prefill_state.argtypes = fwd + [vp]
+    lib.la_prefill_state_ex.argtypes = fwd + [i64p, vp, sz, vp]
+    lib.la_prefill_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32]
+    lib.la_prefill_workspace_size.restype = sz
+    lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
+    lib.la_set_workspace.argtypes = [vp, sz]
+    lib.la_get_last_device_status.argtypes = [vp]
+    lib.la_get_error_string.argtypes = [i32]
+    lib.la_get_error_string.restype = ctypes.c_char_p
+    lib.la_last_launch_count.argtypes = []
+    for name in EXPORTS:
+        f = getattr(lib, name)
+        if f.restype is ctypes.c_int or f.restype is None:
+            f.restype = i32
+    lib.la_causal_fwd_workspace_size.restype = sz
+    lib.la_prefill_workspace_size.restype = sz
+    lib.la_get_error_string.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def error_string(code: int) -> str:
+    return lib.la_get_error_string(int(code)).decode()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream, *tensors):
+    if stream is None:
+        import torch
+        dev = next((t.device for t in tensors if hasattr(t, "device") and t.device.type == "cuda"), None)
+        return torch.cuda.current_stream(dev).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype(dtype, *tensors):
+    if dtype is not None:
+        return int(dtype)
+    import torch
+    t = next(t for t in tensors if hasattr(t, "dtype"))
+    return LA_BF16 if t.dtype == torch.bfloat16 else LA_F32
+
+
+def _check(fn, rc):
+    if rc != LA_OK:
+        raise LinAttnError(fn, rc)
+    return rc
+
+
+def _strides(strides):
+    if strides is None:
+        return None
+    arr = (ctypes.c_int64 * 12)(*[int(s) for s in strides])
+    return arr
+
+
+def la_causal_fwd(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chunk, eps,
+                  dtype=None, stream=None):
+    rc = lib.la_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(M_in), _ptr(z_in), _ptr(M_out),
+                           _ptr(z_out), B, H, T, d, dv, chunk, eps, _dtype(dtype, q), _stream(stream, q))
+    return _check("la_causal_fwd", rc)
+
+
+def la_causal_fwd_ex(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chunk, eps,
+                     dtype=None, strides=None, workspace=None, workspace_bytes=0, stream=None):
+    rc = lib.la_causal_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(M_in), _ptr(z_in), _ptr(M_out),
+                              _ptr(z_out), B, H, T, d, dv, chunk, eps, _dtype(dtype, q), _strides(strides),
+                              _ptr(workspace), int(workspace_bytes), _stream(stream, q))
+    return _check("la_causal_fwd_ex", rc)
+
+
+def la_causal_fwd_workspace_size(B, H, T, d, dv, chunk, dtype) -> int:
+    return int(lib.la_causal_fwd_workspace_size(B, H, T, d, dv, chunk, int(dtype)))
+
+
+def la_prefill_state(q, k, v, out_last, M_in, z_in, M_out, z_out, B, H, T, d, dv, segment, eps,
+                     dtype=None, stream=None):
+    rc = lib.la_prefill_state(_ptr(q), _ptr(k), _ptr(v), _ptr(out_last), _ptr(M_in), _ptr(z_in), _ptr(M_out),
+                              _ptr(z_out), B, H, T, d, dv, segment, eps, _dtype(dtype, q), _stream(stream, q))
+    return _check("la_prefill_state", rc)
+
+
+def la_prefill_state_ex(q, k, v, out_last, M_in, z_in, M_out, z_out, B, H, T, d, dv, segment, eps,
+                        dtype=None, strides=None, workspace=None, workspace_bytes=0, stream=None):
+    rc = lib.la_prefill_state_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out_last), _ptr(M_in), _ptr(z_in),
+                                 _ptr(M_out), _ptr(z_out), B, H, T, d, dv, segment, eps, _dtype(dtype, q),
+                                 _strides(strides), _ptr(workspace), int(workspace_bytes), _stream(stream, q))
+    return _check("la_prefill_state_ex", rc)
+
+
+def la_prefill_workspace_size(B, H, T, d, dv, segment, dtype) -> int:
+    return int(lib.la_prefill_workspace_size(B, H, T, d, dv, segment, int(dtype)))
+
+
+def la_decode_step(q, k, v, out, M, z, N, H, d, dv, eps, dtype=None, stream=None):
+    rc = lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(M), _ptr(z), N, H, d, dv, eps,
+                            _dtype(dtype, q), _stream(stream, q))
+    return _check("la_decode_step", rc)
+
+
+def la_set_workspace(ptr, nbytes):
+    return _check("la_set_workspace", lib.la_set_workspace(_ptr(ptr), int(nbytes)))
+
+
+def la_get_last_device_status(stream=None) -> int:
+    return int(lib.la_get_last_device_status(_stream(stream) if stream is not None else None))
+
+
+def la_get_error_string(code: int) -> str:
+    return error_string(code)
+
+
+def la_last_launch_count() -> int:
+    return int(lib.la_last_launch_count())
+
+
+_workspaces = {}
+
+
+def ensure_workspace(nbytes: int, device=None):
+    """Register a torch-allocated scratch buffer of at least nbytes with the library for
+    `device` (current device by default); kept alive here and grown when needed.
+    Call outside CUDA-graph capture."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    cur = _workspaces.get(dev.index)
+    if cur is not None and cur.numel() >= nbytes:
+        return cur
+    buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        la_set_workspace(buf.data_ptr(), buf.numel())
+    _workspaces[dev.index] = buf
+    return buf

@@ -1,0 +1,479 @@
+// C ABI of the library (declarations and contracts in include/linattn.h):
+// argument validation, path selection, tensor-map construction and launches.
+// Host code only; every step of the computation runs in the kernels of
+// la_simt.cu and la_tc.cu.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/linattn.h"
+#include "la_internal.h"
+
+namespace la {
+
+__device__ int g_status;  // per-device status word (STATUS_* bits), read by la_get_last_device_status
+
+static thread_local int t_launches = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr int kSmemLimit = 227 * 1024;
+
+struct DeviceState {
+    int* status = nullptr;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    int sm_count = 0;
+};
+static DeviceState g_dev[kMaxDevices];
+static std::mutex g_mu;
+
+static int current_device(DeviceState** st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.status) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return LA_ERR_CUDA;
+        s.status = static_cast<int*>(p);
+        cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    }
+    *st = &s;
+    return LA_OK;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D bf16 map {inner, T, H, B} over a strided [B, H, T, inner] tensor; 64 x 64 boxes,
+// 128-byte swizzle (the operand layout the kernels' descriptors assume), zero fill.
+static bool make_map(CUtensorMap* m, const void* base, int inner, int64_t T, int H, int B, int64_t st, int64_t sh,
+                     int64_t sb) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)T, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+    cuuint32_t box[4] = {64, 64, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int env_int(const char* name, int dflt) {
+    const char* s = std::getenv(name);
+    return (s && *s) ? std::atoi(s) : dflt;
+}
+
+static bool shape_ok(int d, int dv) { return d >= 8 && dv >= 8 && d <= 128 && dv <= 128 && d % 8 == 0 && dv % 8 == 0; }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static Strides contiguous(int H, int64_t T, int d, int dv) {
+    Strides s;
+    s.q_st = d, s.q_sh = T * d, s.q_sb = (int64_t)H * T * d;
+    s.k_st = d, s.k_sh = T * d, s.k_sb = (int64_t)H * T * d;
+    s.v_st = dv, s.v_sh = T * dv, s.v_sb = (int64_t)H * T * dv;
+    s.o_st = dv, s.o_sh = T * dv, s.o_sb = (int64_t)H * T * dv;
+    return s;
+}
+
+static Strides from_array(const int64_t* a) {
+    Strides s;
+    s.q_sb = a[0], s.q_sh = a[1], s.q_st = a[2];
+    s.k_sb = a[3], s.k_sh = a[4], s.k_st = a[5];
+    s.v_sb = a[6], s.v_sh = a[7], s.v_st = a[8];
+    s.o_sb = a[9], s.o_sh = a[10], s.o_st = a[11];
+    return s;
+}
+
+static bool strides_valid(const Strides& s, int d, int dv, bool with_out) {
+    const int64_t v[12] = {s.q_sb, s.q_sh, s.q_st, s.k_sb, s.k_sh, s.k_st,
+                           s.v_sb, s.v_sh, s.v_st, s.o_sb, s.o_sh, s.o_st};
+    for (int i = 0; i < (with_out ? 12 : 9); ++i)
+        if (v[i] < 0) return false;
+    return s.q_st >= d && s.k_st >= d && s.v_st >= dv && (!with_out || s.o_st >= dv);
+}
+
+static bool strides_tma(const Strides& s, bool with_out) {
+    const int64_t v[12] = {s.q_sb, s.q_sh, s.q_st, s.k_sb, s.k_sh, s.k_st,
+                           s.v_sb, s.v_sh, s.v_st, s.o_sb, s.o_sh, s.o_st};
+    for (int i = 0; i < (with_out ? 12 : 9); ++i)
+        if (v[i] % 8 != 0 || v[i] * 2 >= (int64_t(1) << 40)) return false;
+    return true;
+}
+
+static int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ forward
+struct FwdPlan {
+    bool tc = false;
+    int nranges = 1;
+    int chunks_per_range = 0;
+    size_t ws_bytes = 0;
+};
+
+static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dtype dtype, int sm_count) {
+    FwdPlan pl;
+    const bool tc_shape = (d == 64 || d == 128) && (dv == 64 || dv == 128) && chunk == 64;
+    pl.tc = dtype == LA_BF16 && tc_shape && env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31);
+    if (!pl.tc) return pl;
+    const int64_t nch = ceil_div(T, 64);
+    const int64_t BH = (int64_t)B * H;
+    int P = env_int("LA_FWD_RANGES", 0);
+    if (P <= 0) P = (int)std::max<int64_t>(1, (sm_count > 0 ? sm_count : 148) / BH);
+    P = (int)std::min<int64_t>(P, nch);
+    const int64_t cpr = ceil_div(nch, P);
+    P = (int)ceil_div(nch, cpr);
+    pl.nranges = P;
+    pl.chunks_per_range = (int)cpr;
+    if (P > 1) {
+        const size_t rec = (size_t)d * dv + d;
+        // records of ranges 0..P-2, plus one per head for a copy of an aliased initial state
+        pl.ws_bytes = sizeof(float) * rec * (size_t)BH * (size_t)P;
+    }
+    return pl;
+}
+
+static int fwd_impl(const void* q, const void* k, const void* v, void* out, const float* M_in, const float* z_in,
+                    float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv, int chunk, float eps,
+                    la_dtype dtype, const int64_t* strides, void* ws, size_t ws_bytes, bool use_registered,
+                    cudaStream_t stream) {
+    t_launches = 0;
+    if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || T <= 0 || !(eps >= 0.f)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+    if (!shape_ok(d, dv)) return LA_ERR_UNSUPPORTED;
+    if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return LA_ERR_UNSUPPORTED;
+    if (out == q || out == k || out == v) return LA_ERR_INVALID_ARG;
+    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return LA_ERR_WORKSPACE;
+    const Strides st = strides ? from_array(strides) : contiguous(H, T, d, dv);
+    if (!strides_valid(st, d, dv, true)) return LA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc) return rc;
+    if (use_registered) ws = ds->ws, ws_bytes = ds->ws_bytes;
+
+    FwdPlan pl = plan_fwd(B, H, T, d, dv, chunk, dtype, ds->sm_count);
+    if (pl.tc && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out) && strides_tma(st, true)))
+        pl.tc = false;
+    if (pl.tc) {
+        if (pl.nranges > 1 && (ws == nullptr || ws_bytes < pl.ws_bytes)) {
+            pl.nranges = 1;  // no scratch: one range per head
+            pl.chunks_per_range = (int)ceil_div(T, 64);
+        }
+        CUtensorMap mq, mk, mv, mo;
+        if (!make_map(&mq, q, d, T, H, B, st.q_st, st.q_sh, st.q_sb) ||
+            !make_map(&mk, k, d, T, H, B, st.k_st, st.k_sh, st.k_sb) ||
+            !make_map(&mv, v, dv, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
+            !make_map(&mo, out, dv, T, H, B, st.o_st, st.o_sh, st.o_sb))
+            return LA_ERR_CUDA;
+        const int64_t BH = (int64_t)B * H;
+        const int64_t rec = (int64_t)d * dv + d;
+        float* wsf = static_cast<float*>(ws);
+        const float* Mi = M_in;
+        const float* zi = z_in;
+        if (pl.nranges > 1) {
+            // ranges other than the last read the initial state while the last writes the
+            // final one: an in-place update needs the initial state copied first
+            float* base = wsf + (size_t)BH * (pl.nranges - 1) * rec;
+            if (M_in && (const void*)M_in == (const void*)M_out) {
+                if (cudaMemcpyAsync(base, M_in, sizeof(float) * BH * d * dv, cudaMemcpyDeviceToDevice, stream))
+                    return LA_ERR_CUDA;
+                Mi = base;
+            }
+            if (z_in && (const void*)z_in == (const void*)z_out) {
+                if (cudaMemcpyAsync(base + BH * d * dv, z_in, sizeof(float) * BH * d, cudaMemcpyDeviceToDevice,
+                                    stream))
+                    return LA_ERR_CUDA;
+                zi = base + BH * d * dv;
+            }
+            PartsParams pp{};
+            pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv;
+            pp.rec_M = rec, pp.rec_z = rec;
+            pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv;
+            pp.part_len = (int64_t)pl.chunks_per_range * 64;
+            pp.nparts = pl.nranges - 1;
+            pp.eps = eps, pp.st = st, pp.status = ds->status;
+            rc = cuda_rc(launch_parts_tc(pp, mk, mv, stream));
+            if (rc) return rc;
+            ++t_launches;
+        }
+        FwdTcParams fp{};
+        fp.M_in = Mi, fp.z_in = zi, fp.M_out = M_out, fp.z_out = z_out;
+        fp.ws = pl.nranges > 1 ? wsf : nullptr;
+        fp.rec = rec, fp.nranges = pl.nranges, fp.chunks_per_range = pl.chunks_per_range;
+        fp.H = H, fp.T = T, fp.eps = eps, fp.status = ds->status;
+        rc = cuda_rc(launch_fwd_tc(fp, d, dv, B, mq, mk, mv, mo, stream));
+        if (!rc) ++t_launches;
+        return rc;
+    }
+    if (fwd_simt_smem(d, dv, chunk) > (size_t)kSmemLimit) return LA_ERR_UNSUPPORTED;
+    FwdParams p{};
+    p.q = q, p.k = k, p.v = v, p.out = out, p.M_in = M_in, p.z_in = z_in, p.M_out = M_out, p.z_out = z_out;
+    p.B = B, p.H = H, p.T = T, p.d = d, p.dv = dv, p.chunk = chunk, p.eps = eps, p.st = st;
+    rc = cuda_rc(launch_fwd_simt(p, dtype == LA_BF16, stream));
+    if (!rc) ++t_launches;
+    return rc;
+}
+
+// ------------------------------------------------------------------ prefill
+struct PrefillPlan {
+    bool tc = false;
+    int64_t part_len = 0;
+    int nparts = 1;
+    size_t parts_bytes = 0;   // per-part records
+    size_t final_bytes = 0;   // final state when M_out / z_out are not given
+};
+
+static PrefillPlan plan_prefill(int B, int H, int64_t T, int d, int dv, int segment, la_dtype dtype) {
+    PrefillPlan pl;
+    const int64_t BH = (int64_t)B * H;
+    const size_t rec = (size_t)d * dv + d;
+    int64_t seg = segment > 0 ? segment : 4096;
+    pl.tc = dtype == LA_BF16 && (d == 64 || d == 128) && (dv == 64 || dv == 128) && seg % 64 == 0 &&
+            env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31);
+    pl.part_len = std::min<int64_t>(seg, T);
+    pl.nparts = (int)ceil_div(T, pl.part_len);
+    pl.parts_bytes = pl.nparts > 1 ? sizeof(float) * rec * BH * pl.nparts : 0;
+    pl.final_bytes = sizeof(float) * rec * BH;
+    return pl;
+}
+
+static int prefill_impl(const void* q, const void* k, const void* v, void* out_last, const float* M_in,
+                        const float* z_in, float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv,
+                        int segment, float eps, la_dtype dtype, const int64_t* strides, void* ws, size_t ws_bytes,
+                        bool use_registered, cudaStream_t stream) {
+    t_launches = 0;
+    if (!q || !k || !v) return LA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || T <= 0 || segment < 0 || !(eps >= 0.f)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+    if (!shape_ok(d, dv)) return LA_ERR_UNSUPPORTED;
+    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return LA_ERR_WORKSPACE;
+    Strides st = strides ? from_array(strides) : contiguous(H, T, d, dv);
+    if (!strides_valid(st, d, dv, false)) return LA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc) return rc;
+    if (use_registered) ws = ds->ws, ws_bytes = ds->ws_bytes;
+    if (!out_last && !M_out && !z_out) return LA_OK;  // nothing requested
+
+    const int64_t BH = (int64_t)B * H;
+    const int64_t rec = (int64_t)d * dv + d;
+    PrefillPlan pl = plan_prefill(B, H, T, d, dv, segment, dtype);
+    if (pl.tc && !(aligned16(k) && aligned16(v) && strides_tma(st, false))) pl.tc = false;
+    const bool need_final = out_last && (!M_out || !z_out);
+    const size_t need = pl.parts_bytes + (need_final ? pl.final_bytes : 0);
+    if (ws_bytes < need || !ws) {
+        // no (or too little) scratch: one part per head, state straight into M_out/z_out
+        pl.nparts = 1;
+        pl.part_len = T;
+        pl.parts_bytes = 0;
+    }
+    float* wsf = static_cast<float*>(ws);
+    const bool have_final_ws = need_final && ws && ws_bytes >= pl.parts_bytes + pl.final_bytes;
+    // where the final state goes
+    float* fM = M_out;
+    float* fz = z_out;
+    if (need_final && have_final_ws) {
+        float* fin = wsf + pl.parts_bytes / sizeof(float);
+        if (!fM) fM = fin;
+        if (!fz) fz = fin + BH * d * dv;
+    }
+    const bool bf16 = dtype == LA_BF16;
+
+    if (need_final && (!fM || !fz)) {
+        // no place for a final state: the SIMT kernel keeps it on chip and reads out itself
+        if (parts_simt_smem(d, dv) > (size_t)kSmemLimit) return LA_ERR_UNSUPPORTED;
+        PartsParams pp{};
+        pp.q = q, pp.k = k, pp.v = v, pp.out_last = out_last, pp.base_M = M_in, pp.base_z = z_in;
+        pp.dst_M = M_out, pp.dst_z = z_out, pp.rec_M = (int64_t)d * dv, pp.rec_z = d;
+        pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv, pp.part_len = T, pp.nparts = 1;
+        pp.eps = eps, pp.st = st, pp.status = ds->status;
+        rc = cuda_rc(launch_parts_simt(pp, bf16, stream));
+        if (!rc) ++t_launches;
+        return rc;
+    }
+
+    CUtensorMap mk, mv;
+    if (pl.tc && (!make_map(&mk, k, d, T, H, B, st.k_st, st.k_sh, st.k_sb) ||
+                  !make_map(&mv, v, dv, T, H, B, st.v_st, st.v_sh, st.v_sb)))
+        return LA_ERR_CUDA;
+
+    PartsParams pp{};
+    pp.q = q, pp.k = k, pp.v = v;
+    pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv, pp.part_len = pl.part_len, pp.nparts = pl.nparts;
+    pp.eps = eps, pp.st = st, pp.status = ds->status;
+    if (pl.nparts == 1) {
+        pp.base_M = M_in, pp.base_z = z_in;
+        pp.dst_M = fM, pp.dst_z = fz, pp.rec_M = (int64_t)d * dv, pp.rec_z = d;
+    } else {
+        pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv, pp.rec_M = rec, pp.rec_z = rec;
+    }
+    if (pl.tc) {
+        if (!pp.dst_M || !pp.dst_z) {
+            // the tensor-core kernel writes both halves of the state; route a missing one to scratch
+            if (!have_final_ws) {
+                if (parts_simt_smem(d, dv) > (size_t)kSmemLimit) return LA_ERR_UNSUPPORTED;
+                pl.tc = false;
+            } else {
+                float* fin = wsf + pl.parts_bytes / sizeof(float);
+                if (!pp.dst_M) pp.dst_M = fin, fM = fin;
+                if (!pp.dst_z) pp.dst_z = fin + BH * d * dv, fz = fin + BH * d * dv;
+            }
+        }
+    }
+    if (pl.tc) {
+        rc = cuda_rc(launch_parts_tc(pp, mk, mv, stream));
+    } else {
+        if (parts_simt_smem(d, dv) > (size_t)kSmemLimit) return LA_ERR_UNSUPPORTED;
+        rc = cuda_rc(launch_parts_simt(pp, bf16, stream));
+    }
+    if (rc) return rc;
+    ++t_launches;
+    if (pl.nparts > 1 && (fM || fz)) {
+        ReduceParams rp{};
+        rp.base_M = M_in, rp.base_z = z_in, rp.parts_M = wsf, rp.parts_z = wsf + (size_t)d * dv;
+        rp.rec_M = rec, rp.rec_z = rec, rp.dst_M = fM, rp.dst_z = fz;
+        rp.BH = (int)BH, rp.d = d, rp.dv = dv, rp.nparts = pl.nparts;
+        if (!fM || !fz) return LA_ERR_INVALID_ARG;  // unreachable: both set when parts > 1
+        rc = cuda_rc(launch_reduce_parts(rp, stream));
+        if (rc) return rc;
+        ++t_launches;
+    }
+    if (out_last) {
+        PrefillOutParams op{};
+        op.q = q, op.out = out_last, op.M = fM, op.z = fz, op.B = B, op.H = H, op.T = T, op.d = d, op.dv = dv;
+        op.eps = eps, op.st = st;
+        rc = cuda_rc(launch_prefill_out(op, bf16, stream));
+        if (rc) return rc;
+        ++t_launches;
+    }
+    return LA_OK;
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+int la_causal_fwd(const void* q, const void* k, const void* v, void* out, const float* M_in, const float* z_in,
+                  float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv, int chunk, float eps,
+                  la_dtype dtype, la_stream_t stream) {
+    return fwd_impl(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chunk, eps, dtype, nullptr, nullptr, 0,
+                    true, (cudaStream_t)stream);
+}
+
+int la_causal_fwd_ex(const void* q, const void* k, const void* v, void* out, const float* M_in, const float* z_in,
+                     float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv, int chunk, float eps,
+                     la_dtype dtype, const int64_t* strides, void* workspace, size_t workspace_bytes,
+                     la_stream_t stream) {
+    return fwd_impl(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chunk, eps, dtype, strides, workspace,
+                    workspace_bytes, false, (cudaStream_t)stream);
+}
+
+size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int chunk, la_dtype dtype) {
+    if (B <= 0 || H <= 0 || T <= 0 || !shape_ok(d, dv)) return 0;
+    int sm = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
+    return plan_fwd(B, H, T, d, dv, chunk, dtype, sm).ws_bytes;
+}
+
+int la_prefill_state(const void* q, const void* k, const void* v, void* out_last, const float* M_in,
+                     const float* z_in, float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv,
+                     int segment, float eps, la_dtype dtype, la_stream_t stream) {
+    return prefill_impl(q, k, v, out_last, M_in, z_in, M_out, z_out, B, H, T, d, dv, segment, eps, dtype, nullptr,
+                        nullptr, 0, true, (cudaStream_t)stream);
+}
+
+int la_prefill_state_ex(const void* q, const void* k, const void* v, void* out_last, const float* M_in,
+                        const float* z_in, float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv,
+                        int segment, float eps, la_dtype dtype, const int64_t* strides, void* workspace,
+                        size_t workspace_bytes, la_stream_t stream) {
+    return prefill_impl(q, k, v, out_last, M_in, z_in, M_out, z_out, B, H, T, d, dv, segment, eps, dtype, strides,
+                        workspace, workspace_bytes, false, (cudaStream_t)stream);
+}
+
+size_t la_prefill_workspace_size(int B, int H, int64_t T, int d, int dv, int segment, la_dtype dtype) {
+    if (B <= 0 || H <= 0 || T <= 0 || !shape_ok(d, dv) || segment < 0) return 0;
+    PrefillPlan pl = plan_prefill(B, H, T, d, dv, segment, dtype);
+    return pl.parts_bytes + pl.final_bytes;
+}
+
+int la_decode_step(const void* q, const void* k, const void* v, void* out, float* M, float* z, int N, int H, int d,
+                   int dv, float eps, la_dtype dtype, la_stream_t stream) {
+    t_launches = 0;
+    if (!q || !k || !v || !out || !M || !z) return LA_ERR_INVALID_ARG;
+    if (N <= 0 || H <= 0 || !(eps >= 0.f)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+    if (!shape_ok(d, dv)) return LA_ERR_UNSUPPORTED;
+    if (!aligned16(M)) return LA_ERR_INVALID_ARG;
+    if (out == q || out == k || out == v) return LA_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc) return rc;
+    DecodeParams p{};
+    p.q = q, p.k = k, p.v = v, p.out = out, p.M = M, p.z = z, p.N = N, p.H = H, p.d = d, p.dv = dv, p.eps = eps;
+    rc = cuda_rc(launch_decode(p, dtype == LA_BF16, (cudaStream_t)stream));
+    if (!rc) ++t_launches;
+    return rc;
+}
+
+int la_set_workspace(void* ptr, size_t bytes) {
+    if (ptr && (reinterpret_cast<uintptr_t>(ptr) & 255u)) return LA_ERR_WORKSPACE;
+    DeviceState* ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lock(g_mu);
+    ds->ws = ptr;
+    ds->ws_bytes = ptr ? bytes : 0;
+    return LA_OK;
+}
+
+int la_get_last_device_status(la_stream_t stream) {
+    DeviceState* ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc) return rc;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ds->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LA_ERR_CUDA;
+    if (v) {
+        const int zero = 0;
+        if (cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    return (v & STATUS_TIMEOUT) ? LA_ERR_TIMEOUT : LA_OK;
+}
+
+const char* la_get_error_string(int code) {
+    switch (code) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument";
+        case LA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case LA_ERR_CUDA: return "CUDA runtime or launch failure";
+        case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        case LA_ERR_WORKSPACE: return "workspace pointer not 256-byte aligned";
+        default: return "unknown error";
+    }
+}
+
+int la_last_launch_count(void) { return t_launches; }
+
+}  // extern "C"

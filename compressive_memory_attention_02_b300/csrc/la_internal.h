@@ -1,0 +1,127 @@
+// Internal parameter blocks and launchers shared by the kernel files and the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "la_ptx.cuh"
+
+namespace la {
+
+// Element strides (innermost stride is 1) of q, k, v and out in [B, H, T, .].
+struct Strides {
+    int64_t q_sb, q_sh, q_st;
+    int64_t k_sb, k_sh, k_st;
+    int64_t v_sb, v_sh, v_st;
+    int64_t o_sb, o_sh, o_st;
+};
+
+struct FwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    const float* M_in;
+    const float* z_in;
+    float* M_out;
+    float* z_out;
+    int B, H;
+    int64_t T;
+    int d, dv, chunk;
+    float eps;
+    Strides st;
+};
+
+// Per-part state sums. Record (bh, p) is at dst_M + (bh*nparts + p)*rec_M (d x dv,
+// row-major) and dst_z + (bh*nparts + p)*rec_z (d).
+struct PartsParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out_last;        // SIMT kernel only, nparts == 1: read-out of the last token
+    const float* base_M;   // added to every record (used with nparts == 1), may be null
+    const float* base_z;
+    float* dst_M;
+    float* dst_z;
+    int64_t rec_M, rec_z;
+    int B, H;
+    int64_t T;
+    int d, dv;
+    int64_t part_len;
+    int nparts;
+    float eps;
+    Strides st;
+    int* status;
+};
+
+struct ReduceParams {
+    const float* base_M;   // may be null (zero state)
+    const float* base_z;
+    const float* parts_M;
+    const float* parts_z;
+    int64_t rec_M, rec_z;
+    float* dst_M;
+    float* dst_z;
+    int BH, d, dv, nparts;
+};
+
+struct PrefillOutParams {
+    const void* q;
+    void* out;
+    const float* M;
+    const float* z;
+    int B, H;
+    int64_t T;
+    int d, dv;
+    float eps;
+    Strides st;
+};
+
+struct DecodeParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    float* M;
+    float* z;
+    int N, H, d, dv;
+    float eps;
+};
+
+// Tensor-core forward: one block per (range, b*H + h).
+struct FwdTcParams {
+    const float* M_in;
+    const float* z_in;
+    float* M_out;
+    float* z_out;
+    const float* ws;       // range aggregates from parts_tc (records of all ranges but the last)
+    int64_t rec;           // floats per record (d*dv + d); M at +0, z at +d*dv
+    int nranges;
+    int chunks_per_range;
+    int H;
+    int64_t T;
+    float eps;
+    int* status;
+};
+
+// device status word bits
+enum : int { STATUS_TIMEOUT = 1 };
+
+// SIMT launchers (la_simt.cu)
+size_t fwd_simt_smem(int d, int dv, int C);
+size_t parts_simt_smem(int d, int dv);
+cudaError_t launch_fwd_simt(const FwdParams& p, bool bf16, cudaStream_t s);
+cudaError_t launch_parts_simt(const PartsParams& p, bool bf16, cudaStream_t s);
+cudaError_t launch_reduce_parts(const ReduceParams& p, cudaStream_t s);
+cudaError_t launch_prefill_out(const PrefillOutParams& p, bool bf16, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
+
+// Tensor-core launchers (la_tc.cu). Maps are 4-D bf16 tensor maps {inner, T, H, B}
+// with 64 x 64 boxes and 128-byte swizzle.
+cudaError_t launch_parts_tc(const PartsParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s);
+cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s);
+
+}  // namespace la

@@ -1,0 +1,155 @@
+/*
+ * linattn — causal linear attention (Katharopoulos form, phi = elu + 1) for
+ * NVIDIA B300 (sm_103a). C ABI: plain pointers and sizes only.
+ *
+ * The method (page "Attention_Kernel_Mask", allenlu2009.github.io, section
+ * "Implementing Causality with Cumulative Sums"):
+ *     z_t = z_{t-1} + phi(k_t)                 key sum, d
+ *     M_t = M_{t-1} + phi(k_t) v_t^T           memory, d x dv
+ *     out_t = phi(q_t)^T M_t / (phi(q_t)^T z_t + eps)
+ * with one (M, z) per (batch, head), carried across calls as the compressive
+ * memory of the page "Segment-Wise Attention" (github.com/beomi/infinitransformer,
+ * issue 2). The three modes of the first page's table "Causal Attention
+ * Training and Inferencing" are the three entry points: training forward (all
+ * outputs), prompt/prefill (state plus last output) and generation (one step).
+ *
+ * Layouts (the [batch, heads, seq, head_dim] order of the KERPLE page's
+ * Hugging Face attention code): q, k [B, H, T, d]; v, out [B, H, T, dv];
+ * element (b, h, t, i) at b*sb + h*sh + t*st + i (contiguous: st = d or dv,
+ * sh = T*st, sb = H*sh). State M [B, H, d, dv] float32 row-major, z [B, H, d]
+ * float32, always contiguous.
+ *
+ * Ownership: the caller owns every buffer. All data pointers are DEVICE
+ * pointers unless a parameter says otherwise. No call allocates device
+ * memory. Scratch for the parallel schedules comes from a caller workspace
+ * (the *_ex calls' `workspace`, or the buffer registered with
+ * la_set_workspace for the plain calls); without one, the calls still run,
+ * on schedules that need no scratch (one thread block per (batch, head)
+ * carries that head's state through all T tokens).
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and never synchronise. They return LA_OK or an error code for
+ * problems found on the host before any launch; nothing is launched when a
+ * call returns an error. Problems found on the device (a bounded wait that ran
+ * out) are recorded in a per-device status word read by
+ * la_get_last_device_status.
+ *
+ * Supported: dtype LA_F32 or LA_BF16 for q/k/v/out (same type for all four;
+ * state is always float32); 1 <= d, dv <= 128 with d, dv multiples of 8;
+ * T >= 1; chunk in {16, 32, 64, 128}. The bf16 tensor-core path takes
+ * d, dv in {64, 128}, chunk 64, 16-byte aligned pointers and strides that are
+ * multiples of 8 elements; other bf16 shapes run on the SIMT path.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* la_stream_t; /* identical to cudaStream_t */
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,   /* null/aliasing pointers, non-positive sizes, bad strides */
+    LA_ERR_UNSUPPORTED = 2,   /* d, dv, chunk or dtype outside the supported set */
+    LA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
+    LA_ERR_TIMEOUT = 4,       /* device status: a bounded wait inside a kernel ran out */
+    LA_ERR_WORKSPACE = 5      /* workspace pointer misaligned */
+};
+
+/* ---- training forward (mode 3 of the mode table: all outputs) -------------
+ * Chunk-sequential form of the page's equation for "chunk sequential mode":
+ * per chunk of `chunk` tokens, out = (phi(Q_c) M_{c-1} + ((phi(Q_c) phi(K_c)^T) o mask) V_c)
+ * / (phi(Q_c) z_{c-1} + rowsum((phi(Q_c) phi(K_c)^T) o mask) + eps), mask = lower
+ * triangle with diagonal; then M_c = M_{c-1} + phi(K_c)^T V_c, z_c = z_{c-1} + sum phi(K_c).
+ *   q, k     [B,H,T,d]  dtype, read
+ *   v        [B,H,T,dv] dtype, read
+ *   out      [B,H,T,dv] dtype, written (all T outputs); must not alias q, k, v
+ *   M_in,z_in  initial state [B,H,d,dv] / [B,H,d] float32, read; NULL = zero state
+ *   M_out,z_out final state, written; NULL = not written; M_out may equal M_in
+ *              (and z_out z_in): the update is then in place
+ *   chunk    intra-chunk block length; eps > 0 added to every denominator. */
+int la_causal_fwd(const void* q, const void* k, const void* v, void* out,
+                  const float* M_in, const float* z_in, float* M_out, float* z_out,
+                  int B, int H, int64_t T, int d, int dv, int chunk, float eps,
+                  la_dtype dtype, la_stream_t stream);
+
+/* As la_causal_fwd, plus:
+ *   strides    HOST pointer to 12 int64 element strides, or NULL for contiguous:
+ *              {q_sb, q_sh, q_st, k_sb, k_sh, k_st, v_sb, v_sh, v_st, o_sb, o_sh, o_st}
+ *              (innermost stride is 1). Lets a caller run one segment of a longer
+ *              [B,H,T_total,d] tensor in place (the segment-wise use of the
+ *              "Segment-Wise Attention" page) without copies.
+ *   workspace  device scratch of workspace_bytes (256-byte aligned), or NULL/0.
+ *              la_causal_fwd_workspace_size() gives the size that enables the
+ *              sequence-split schedule; with less, the single-range schedule runs. */
+int la_causal_fwd_ex(const void* q, const void* k, const void* v, void* out,
+                     const float* M_in, const float* z_in, float* M_out, float* z_out,
+                     int B, int H, int64_t T, int d, int dv, int chunk, float eps,
+                     la_dtype dtype, const int64_t* strides,
+                     void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int chunk,
+                                    la_dtype dtype);
+
+/* ---- prefill (prompt mode: state plus last output) ---------------------------
+ * Only the final state and the last token's output, as the mode table's note
+ * on the prompt mode says ("only S_n ... output in the last block"); the key-
+ * value sums are formed in parallel parts of `segment` tokens (the page's
+ * remark that the sum can be done in parallel, e.g. as a tree) and added in
+ * part order to M_in:  M_T = M_in + sum_p sum_{t in p} phi(k_t) v_t^T,
+ * z_T = z_in + sum phi(k_t), out_last = phi(q_T)^T M_T / (phi(q_T)^T z_T + eps).
+ *   out_last  [B,H,dv] dtype, written (may be NULL)
+ *   M_out, z_out  written (may be NULL); M_out may equal M_in
+ *   segment   tokens per part (0 = library choice). */
+int la_prefill_state(const void* q, const void* k, const void* v, void* out_last,
+                     const float* M_in, const float* z_in, float* M_out, float* z_out,
+                     int B, int H, int64_t T, int d, int dv, int segment, float eps,
+                     la_dtype dtype, la_stream_t stream);
+
+int la_prefill_state_ex(const void* q, const void* k, const void* v, void* out_last,
+                        const float* M_in, const float* z_in, float* M_out, float* z_out,
+                        int B, int H, int64_t T, int d, int dv, int segment, float eps,
+                        la_dtype dtype, const int64_t* strides,
+                        void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+size_t la_prefill_workspace_size(int B, int H, int64_t T, int d, int dv, int segment,
+                                 la_dtype dtype);
+
+/* ---- generation (pure sequential mode: one recurrent step) -----------------
+ * For N independent streams x H heads, one token each:
+ *   M <- M + phi(k) v^T;  z <- z + phi(k);  out = phi(q)^T M / (phi(q)^T z + eps)
+ *   q, k [N,H,d], v [N,H,dv] dtype contiguous, read
+ *   out  [N,H,dv] dtype, written
+ *   M [N,H,d,dv], z [N,H,d] float32, read and written in place. */
+int la_decode_step(const void* q, const void* k, const void* v, void* out,
+                   float* M, float* z, int N, int H, int d, int dv, float eps,
+                   la_dtype dtype, la_stream_t stream);
+
+/* ---- runtime -------------------------------------------------------------------
+ * la_set_workspace: register (ptr, bytes) as the scratch of the plain calls on
+ * the CURRENT device (the caller keeps ownership; NULL/0 unregisters). The
+ * buffer must stay valid until the last call that may use it has completed,
+ * and calls that share it must be ordered (same stream or synchronised). */
+int la_set_workspace(void* ptr, size_t bytes);
+
+/* Reads and clears this device's status word; synchronises `stream` first.
+ * Returns LA_OK or the first device-side error recorded since the last read. */
+int la_get_last_device_status(la_stream_t stream);
+
+const char* la_get_error_string(int code);
+
+/* Number of kernels the most recent call on this host thread launched. */
+int la_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */
