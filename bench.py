@@ -76,8 +76,53 @@ def peaks():
 
 # ----------------------------------------------------------------------------- clocks
 
+class _Nvml:
+    """Minimal ctypes binding of the NVML calls the sampler needs (libnvidia-ml ships
+    with the driver; the pynvml wrapper may not be installed)."""
+    SM = 1  # NVML_CLOCK_SM
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        handle = None
+        try:  # the device CUDA calls cuda_index, found by PCI bus id
+            import torch
+            p = torch.cuda.get_device_properties(cuda_index)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) == 0:
+                handle = self.h
+        except Exception:
+            handle = None
+        if handle is None:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = int(vis.split(",")[cuda_index]) if vis and vis.split(",")[cuda_index].isdigit() else cuda_index
+            if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def clock(self, maximum=False):
+        v = self.c.c_uint()
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if maximum else self.lib.nvmlDeviceGetClockInfo
+        if fn(self.h, self.SM, self.c.byref(v)) != 0:
+            raise RuntimeError("clock query failed")
+        return int(v.value)
+
+    def reasons(self):
+        v = self.c.c_ulonglong()
+        if self.reasons_fn(self.h, self.c.byref(v)) != 0:
+            raise RuntimeError("reasons query failed")
+        return int(v.value)
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+    """Samples SM clock and clock-event (throttle) reasons through NVML, every ~2 ms,
+    while the timed region runs."""
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
         0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
@@ -85,29 +130,26 @@ class ClockSampler:
     }
 
     def __init__(self, index):
-        self.samples, self.reasons, self.ok = [], set(), False
+        self.samples, self.reasons, self.ok, self.error = [], set(), False, None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nv = _Nvml(index)
+            self.max_mhz = self.nv.clock(maximum=True)
             self.ok = True
-        except Exception:
+        except Exception as e:  # NVML unavailable: report why
             self.max_mhz = None
+            self.error = f"{type(e).__name__}: {e}"
         self._stop = threading.Event()
 
     def _run(self):
-        nv = self.nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append(self.nv.clock())
+                r = self.nv.reasons()
                 for bit, name in self.REASONS.items():
                     if r & bit and name != "gpu_idle":
                         self.reasons.add(name)
-            except Exception:
-                pass
+            except Exception as e:
+                self.error = f"{type(e).__name__}: {e}"
             time.sleep(0.002)
 
     def __enter__(self):
@@ -122,8 +164,11 @@ class ClockSampler:
             self.t.join()
 
     def summary(self):
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        if self.error and not self.samples:
+            out["error"] = self.error
+        return out
 
 
 # ----------------------------------------------------------------------------- inputs

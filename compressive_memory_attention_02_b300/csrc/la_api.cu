@@ -1,7 +1,7 @@
 // C ABI of the library (declarations and contracts in include/linattn.h):
 // argument validation, path selection, tensor-map construction and launches.
 // Host code only; every step of the computation runs in the kernels of
-// la_simt.cu and la_tc.cu.
+// la_simt.cu, la_tc.cu and la_fwd_tc.cu.
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
@@ -122,32 +122,54 @@ static int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUD
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------------ forward
+// Schedules of the tensor-core forward (per head, the chunks are split into ranges
+// that run on different SMs):
+//   single  one range per head (B*H fills the GPU, or no scratch for an aliased state)
+//   fused2  two ranges; range 1 forms the state of range 0's chunks itself
+//   parts   P > 2 ranges; parts_tc writes the state sum of each range but the last
+//           to the workspace, and range r starts from M_in plus those of ranges < r
 struct FwdPlan {
     bool tc = false;
     int nranges = 1;
     int chunks_per_range = 0;
-    size_t ws_bytes = 0;
+    int split = 0;
+    size_t ws_bytes = 0;      // scratch that enables the plan (0: none needed)
 };
 
-static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dtype dtype, int sm_count) {
+static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dtype dtype, int sm_count,
+                        bool aliased, size_t ws_avail) {
     FwdPlan pl;
     const bool tc_shape = (d == 64 || d == 128) && (dv == 64 || dv == 128) && chunk == 64;
     pl.tc = dtype == LA_BF16 && tc_shape && env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31);
     if (!pl.tc) return pl;
     const int64_t nch = ceil_div(T, 64);
     const int64_t BH = (int64_t)B * H;
+    const size_t rec_bytes = sizeof(float) * ((size_t)d * dv + d) * (size_t)BH;
     int P = env_int("LA_FWD_RANGES", 0);
     if (P <= 0) P = (int)std::max<int64_t>(1, (sm_count > 0 ? sm_count : 148) / BH);
     P = (int)std::min<int64_t>(P, nch);
-    const int64_t cpr = ceil_div(nch, P);
-    P = (int)ceil_div(nch, cpr);
-    pl.nranges = P;
-    pl.chunks_per_range = (int)cpr;
-    if (P > 1) {
-        const size_t rec = (size_t)d * dv + d;
-        // records of ranges 0..P-2, plus one per head for a copy of an aliased initial state
-        pl.ws_bytes = sizeof(float) * rec * (size_t)BH * (size_t)P;
+    pl.chunks_per_range = (int)nch;
+    if (P <= 1) return pl;
+    const size_t alias_bytes = aliased ? rec_bytes : 0;   // copy of M_in/z_in read by every range
+    if (P > 2) {
+        const int64_t cpr = ceil_div(nch, P);
+        const int P2 = (int)ceil_div(nch, cpr);
+        const size_t need = rec_bytes * (size_t)(P2 - 1) + alias_bytes;
+        if (P2 > 2 && ws_avail >= need) {
+            pl.nranges = P2;
+            pl.chunks_per_range = (int)cpr;
+            pl.ws_bytes = need;
+            return pl;
+        }
+        P = 2;
     }
+    if (ws_avail < alias_bytes) return pl;
+    const int pct = env_int("LA_FWD_SPLIT_PCT", 58);
+    int64_t split = (nch * pct + 50) / 100;
+    split = std::max<int64_t>(1, std::min<int64_t>(split, nch - 1));
+    pl.nranges = 2;
+    pl.split = (int)split;
+    pl.ws_bytes = alias_bytes;
     return pl;
 }
 
@@ -169,15 +191,14 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
     int rc = current_device(&ds);
     if (rc) return rc;
     if (use_registered) ws = ds->ws, ws_bytes = ds->ws_bytes;
+    if (!ws) ws_bytes = 0;
 
-    FwdPlan pl = plan_fwd(B, H, T, d, dv, chunk, dtype, ds->sm_count);
+    const bool aliased = (M_in && (const void*)M_in == (const void*)M_out) ||
+                         (z_in && (const void*)z_in == (const void*)z_out);
+    FwdPlan pl = plan_fwd(B, H, T, d, dv, chunk, dtype, ds->sm_count, aliased, ws_bytes);
     if (pl.tc && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out) && strides_tma(st, true)))
         pl.tc = false;
     if (pl.tc) {
-        if (pl.nranges > 1 && (ws == nullptr || ws_bytes < pl.ws_bytes)) {
-            pl.nranges = 1;  // no scratch: one range per head
-            pl.chunks_per_range = (int)ceil_div(T, 64);
-        }
         CUtensorMap mq, mk, mv, mo;
         if (!make_map(&mq, q, d, T, H, B, st.q_st, st.q_sh, st.q_sb) ||
             !make_map(&mk, k, d, T, H, B, st.k_st, st.k_sh, st.k_sb) ||
@@ -189,10 +210,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
         float* wsf = static_cast<float*>(ws);
         const float* Mi = M_in;
         const float* zi = z_in;
-        if (pl.nranges > 1) {
-            // ranges other than the last read the initial state while the last writes the
-            // final one: an in-place update needs the initial state copied first
-            float* base = wsf + (size_t)BH * (pl.nranges - 1) * rec;
+        if (pl.nranges > 1 && aliased) {
+            // every range reads the initial state while the last one writes the final
+            // state in place: read the initial state from a copy
+            float* base = wsf + (pl.nranges > 2 ? (size_t)BH * (pl.nranges - 1) * rec : 0);
             if (M_in && (const void*)M_in == (const void*)M_out) {
                 if (cudaMemcpyAsync(base, M_in, sizeof(float) * BH * d * dv, cudaMemcpyDeviceToDevice, stream))
                     return LA_ERR_CUDA;
@@ -204,6 +225,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
                     return LA_ERR_CUDA;
                 zi = base + BH * d * dv;
             }
+        }
+        if (pl.nranges > 2) {
             PartsParams pp{};
             pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv;
             pp.rec_M = rec, pp.rec_z = rec;
@@ -217,8 +240,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
         }
         FwdTcParams fp{};
         fp.M_in = Mi, fp.z_in = zi, fp.M_out = M_out, fp.z_out = z_out;
-        fp.ws = pl.nranges > 1 ? wsf : nullptr;
-        fp.rec = rec, fp.nranges = pl.nranges, fp.chunks_per_range = pl.chunks_per_range;
+        fp.ws = pl.nranges > 2 ? wsf : nullptr;
+        fp.rec = rec, fp.nranges = pl.nranges, fp.chunks_per_range = pl.chunks_per_range, fp.split = pl.split;
         fp.H = H, fp.T = T, fp.eps = eps, fp.status = ds->status;
         rc = cuda_rc(launch_fwd_tc(fp, d, dv, B, mq, mk, mv, mo, stream));
         if (!rc) ++t_launches;
@@ -394,7 +417,8 @@ size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int 
     int sm = 148;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
-    return plan_fwd(B, H, T, d, dv, chunk, dtype, sm).ws_bytes;
+    // the largest scratch any plan for this shape may use (an in-place state included)
+    return plan_fwd(B, H, T, d, dv, chunk, dtype, sm, true, SIZE_MAX).ws_bytes;
 }
 
 int la_prefill_state(const void* q, const void* k, const void* v, void* out_last, const float* M_in,

@@ -1,0 +1,492 @@
+// Tensor-core chunk-sequential causal forward for bf16 storage, f32 accumulation:
+// the "chunk sequential mode" (mode 3) of the page "Attention_Kernel_Mask"
+// (allenlu2009.github.io), with the normaliser of that page's cumulative-sum
+// recurrence split the same way. Per chunk c of 64 tokens:
+//     S'  = phi(Q_c) [phi(K_c) ; z_{c-1}]^T              64 x 80 (TMEM)
+//     P   = S'[:, :64] masked to the lower triangle incl. the diagonal (bf16, smem)
+//     den = S'[:, 64] + rowsum(P) + eps                   (= phi(q_t).z_t + eps)
+//     O^T = M_{c-1}^T phi(Q_c)^T + V_c^T P^T              dv x 64 (TMEM)
+//     out = O / den
+//     M^T += V_c^T phi(K_c) (f32 in TMEM),  z += colsum(phi(K_c)) (f32)
+// M^T is re-cast to bf16 in shared memory after every update, as the A operand of
+// the next chunk's inter-chunk MMA.
+//
+// One block per (range, head). Warp roles (512 threads):
+//   warp 0        TMA producer: Q, K, V tiles into a 3-stage ring
+//   warp 1        TMEM owner; lane 0 issues every tcgen05.mma, software-pipelined
+//                 one chunk ahead: PV_c, then S'_{c+1}, inter_{c+1}, update_{c+1}
+//   warps 2,3,14,15  F: phi in place on Q and K, zero padded keys, column sums -> z
+//   warps 4-7     R: initial state into TMEM; bf16 re-cast of M after each update;
+//                 final M to global memory
+//   warps 8-11    E: out = O / den -> swizzled smem tile -> TMA store
+//   warps 12,13   S: P and 1/den from S'
+// A warp touches only its TMEM lane quarter (warp % 4). Each hand-off is an
+// mbarrier; TMEM reads and writes are ordered with tcgen05 fences around it.
+//
+// Sequence split: in the fused two-range schedule (split > 0) range 1 first forms
+// the state of chunks [0, split) itself (phi(K) and the update only) while range 0
+// runs its main pass over the same chunks; in the parts schedule range r adds the
+// aggregates of ranges < r written by parts_tc.
+//
+// Operand layouts (128-byte swizzle, 1024-byte aligned atoms, 16-byte chunk c of row
+// r at chunk c ^ (r % 8)): Q, K, V tiles as TMA loads them ([64 tokens][64 features]
+// per atom; K atoms have 16 extra rows: row 64 holds bf16 z_{c-1}, rows 65-79 zero);
+// phi(Q), phi(K) read K-major for S' and inter; phi(K), V read MN-major (K = tokens)
+// for the update and PV; P [64 queries][64 keys] K-major; M^T bf16 [128][d] K-major.
+#include "la_tc_common.cuh"
+
+namespace la {
+
+template <int D, int DV>
+struct FwdLayout {
+    static constexpr int NST = 3;
+    static constexpr int QB = D / 64 * ATOM;
+    static constexpr int KB = D / 64 * ATOMK;
+    static constexpr int VB = DV / 64 * ATOM;
+    static constexpr int Q0 = 0;
+    static constexpr int K0 = Q0 + NST * QB;     // an M=128 read past the last Q atom lands here
+    static constexpr int V0 = K0 + NST * KB;
+    static constexpr int MT = V0 + NST * VB;     // an M=128 read past a 64-wide V tile lands here
+    static constexpr int MTB = D / 64 * (128 * 128);
+    static constexpr int PT = MT + MTB;          // P, two buffers
+    static constexpr int OT = PT + 2 * ATOM;     // out tile
+    static constexpr int SMALL = OT + DV / 64 * ATOM;
+    static constexpr int RDEN = SMALL;           // 2 x 64 floats
+    static constexpr int ZF = RDEN + 2 * 64 * 4;  // 128 floats
+    static constexpr int ZP = ZF + 128 * 4;      // 2 x 4 x D floats
+    static constexpr int BAR = ZP + 2 * 4 * D * 4;
+    static constexpr int NBAR = 22;
+    static constexpr int MISC = BAR + 8 * NBAR;
+    static constexpr int TOTAL = MISC + 16;
+    static constexpr int ALLOC = TOTAL + 1024;
+};
+
+// TMEM column map (512 columns allocated)
+constexpr uint32_t TM_M = 0;                                                      // M^T f32, d columns
+__device__ __forceinline__ uint32_t tm_s(int buf) { return 128u + 80u * buf; }  // S', 80 columns each
+__device__ __forceinline__ uint32_t tm_o(int buf) { return 288u + 64u * buf; }  // O^T, 64 columns each
+
+template <int D, int DV>
+__global__ void __launch_bounds__(512, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, FwdTcParams p) {
+    using L = FwdLayout<D, DV>;
+    constexpr int NST = L::NST;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    float* rden = reinterpret_cast<float*>(sm + L::RDEN);
+    float* zf = reinterpret_cast<float*>(sm + L::ZF);
+    float* zpart = reinterpret_cast<float*>(sm + L::ZP);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+    uint64_t* full = bars + 0;      // [3] TMA landed
+    uint64_t* empty = bars + 3;     // [3] stage free (MMA commit)
+    uint64_t* phib = bars + 6;      // [3] phi applied (F)
+    uint64_t* s_full = bars + 9;    // [2] S' ready (MMA commit)
+    uint64_t* s_free = bars + 11;   // [2] S' read (S)
+    uint64_t* p_full = bars + 13;   // [2] P and 1/den written (S)
+    uint64_t* o_full = bars + 15;   // [2] O^T ready (MMA commit)
+    uint64_t* o_free = bars + 17;   // [2] O^T and 1/den read (E)
+    uint64_t* upd_done = bars + 19; // state update finished (MMA commit)
+    uint64_t* mt_ready = bars + 20; // bf16 M^T written and TMEM M read (R)
+    uint64_t* drain = bars + 21;    // all MMAs finished (MMA thread only)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / p.H, h = bh % p.H;
+    const int nch = (int)((p.T + CH - 1) / CH);
+    int main_begin, main_end, n_agg = 0, nws = 0;
+    if (p.split > 0) {
+        main_begin = r == 0 ? 0 : p.split;
+        main_end = r == 0 ? p.split : nch;
+        n_agg = r == 0 ? 0 : p.split;
+    } else {
+        main_begin = r * p.chunks_per_range;
+        main_end = min(nch, main_begin + p.chunks_per_range);
+        nws = r;
+    }
+    const int n_main = main_end - main_begin;
+    const int nchunks = n_agg + n_main;            // chunks streamed through the ring
+    const bool writes_state = (r == p.nranges - 1);
+    const float* agg = p.ws ? p.ws + (int64_t)bh * (p.nranges - 1) * p.rec : nullptr;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < L::NBAR; ++i) mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+        tma_prefetch_desc(&mo);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ======================================================== TMA producer
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();  // q, k, v are read once
+            int issued = 0;
+            for (int g = 0; g < nchunks; ++g) {
+                const int s = g % NST;
+                if (g >= NST && !mbar_wait(&empty[s], ((g / NST) - 1) & 1, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    break;
+                }
+                const bool is_main = g >= n_agg;
+                const int t = (is_main ? main_begin + g - n_agg : g) * CH;
+                mbar_expect_tx(&full[s], ((is_main ? D : 0) + D + DV) * CH * 2);
+#pragma unroll
+                for (int a = 0; a < D / 64; ++a) {
+                    if (is_main)
+                        tma_load_4d_hint(sm + L::Q0 + s * L::QB + a * ATOM, &mq, &full[s], a * 64, t, h, b, pol);
+                    tma_load_4d_hint(sm + L::K0 + s * L::KB + a * ATOMK, &mk, &full[s], a * 64, t, h, b, pol);
+                }
+#pragma unroll
+                for (int a = 0; a < DV / 64; ++a)
+                    tma_load_4d_hint(sm + L::V0 + s * L::VB + a * ATOM, &mv, &full[s], a * 64, t, h, b, pol);
+                ++issued;
+            }
+            for (int g = max(0, issued - NST); g < issued; ++g) mbar_wait_drain(&full[g % NST], (g / NST) & 1);
+        }
+    } else if (warp == 1) {
+        // ======================================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16(128, KROWS, 0, 0);  // S' = phiQ [phiK; z]^T
+            constexpr uint32_t id_u = idesc_bf16(128, D, 1, 1);      // M^T += V^T phiK
+            constexpr uint32_t id_pv = idesc_bf16(128, CH, 1, 0);    // O^T += V^T P^T
+            constexpr uint32_t id_in = idesc_bf16(128, CH, 0, 0);    // O^T = M^T phiQ^T
+            const uint32_t q0 = smem_u32(sm + L::Q0), k0 = smem_u32(sm + L::K0), v0 = smem_u32(sm + L::V0);
+            const uint32_t mt = smem_u32(sm + L::MT), pt = smem_u32(sm + L::PT);
+            bool ok = true;
+            int mt_waits = 0;
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                if (ok && !mbar_wait(bar, parity, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    ok = false;
+                }
+                return ok;
+            };
+            auto update = [&](int s) {
+                const uint32_t vb = v0 + s * L::VB, kb = k0 + s * L::KB;
+#pragma unroll
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    mma_bf16_ss(tmem + TM_M, sdesc_sw128(vb + ks * 2048, ATOM, 1024),
+                                sdesc_sw128(kb + ks * 2048, ATOMK, 1024), id_u, 1);
+            };
+            // S'_m, inter_m, update_m of main chunk m
+            auto front = [&](int m) {
+                const int g = n_agg + m, s = g % NST, buf = m & 1;
+                const uint32_t qb = q0 + s * L::QB, kb = k0 + s * L::KB;
+                if (!wait(&phib[s], (g / NST) & 1)) return false;
+                if (m >= 2 && !wait(&s_free[buf], ((m >> 1) - 1) & 1)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;
+                    mma_bf16_ss(tmem + tm_s(buf), sdesc_sw128(qb + (ks >> 2) * ATOM + off, 16, 1024),
+                                sdesc_sw128(kb + (ks >> 2) * ATOMK + off, 16, 1024), id_s, ks != 0);
+                }
+                mma_commit(&s_full[buf]);
+                if (!wait(mt_ready, mt_waits++ & 1)) return false;
+                if (m >= 2 && !wait(&o_free[buf], ((m >> 1) - 1) & 1)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;
+                    mma_bf16_ss(tmem + tm_o(buf), sdesc_sw128(mt + (ks >> 2) * (128 * 128) + off, 16, 1024),
+                                sdesc_sw128(qb + (ks >> 2) * ATOM + off, 16, 1024), id_in, ks != 0);
+                }
+                update(s);
+                mma_commit(upd_done);
+                return true;
+            };
+            if (n_agg > 0) {
+                wait(mt_ready, mt_waits++ & 1);  // initial state in TMEM
+                tc_fence_after();
+                for (int g = 0; ok && g < n_agg; ++g) {
+                    const int s = g % NST;
+                    if (!wait(&phib[s], (g / NST) & 1)) break;
+                    tc_fence_after();
+                    update(s);
+                    mma_commit(&empty[s]);
+                }
+                if (ok) mma_commit(upd_done);
+            }
+            if (ok && n_main > 0) front(0);
+            for (int m = 0; ok && m < n_main; ++m) {
+                const int g = n_agg + m, s = g % NST, buf = m & 1;
+                if (!wait(&p_full[buf], (m >> 1) & 1)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    mma_bf16_ss(tmem + tm_o(buf), sdesc_sw128(v0 + s * L::VB + ks * 2048, ATOM, 1024),
+                                sdesc_sw128(pt + buf * ATOM + ks * 32, 16, 1024), id_pv, 1);
+                mma_commit(&o_full[buf]);
+                mma_commit(&empty[s]);
+                if (m + 1 < n_main && !front(m + 1)) break;
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ======================================================== R: state
+        const int ct = threadIdx.x - 128;
+        const int q = warp & 3;
+        const int j = 32 * q + lane;              // dv row of M^T
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const bool has_row = 32 * q < DV;         // warp-uniform
+        uint8_t* mrow = sm + L::MT + j * 128;
+        auto store_bf16_row = [&](int i0, const uint32_t* x) {  // 32 f32 values, columns i0..i0+31
+            uint8_t* atom = mrow + (i0 >> 6) * (128 * 128);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int cc = ((i0 & 63) >> 3) + u;
+                const uint32_t* y = x + 8 * u;
+                *reinterpret_cast<uint4*>(atom + ((cc ^ (j & 7)) << 4)) =
+                    make_uint4(pack_bf16(__uint_as_float(y[0]), __uint_as_float(y[1])),
+                               pack_bf16(__uint_as_float(y[2]), __uint_as_float(y[3])),
+                               pack_bf16(__uint_as_float(y[4]), __uint_as_float(y[5])),
+                               pack_bf16(__uint_as_float(y[6]), __uint_as_float(y[7])));
+            }
+        };
+        if (has_row) {
+#pragma unroll 1
+            for (int i0 = 0; i0 < D; i0 += 32) {
+                uint32_t x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int i = i0 + e;
+                    float m = p.M_in ? __ldg(p.M_in + ((int64_t)bh * D + i) * DV + j) : 0.f;
+                    for (int pp = 0; pp < nws; ++pp) m += __ldg(agg + pp * p.rec + i * DV + j);
+                    x[e] = __float_as_uint(m);
+                }
+                tmem_st16(tmem + TM_M + lane_base + i0, x);
+                tmem_st16(tmem + TM_M + lane_base + i0 + 16, x + 16);
+                store_bf16_row(i0, x);
+            }
+            tmem_wait_st();
+        } else {
+            for (int a = 0; a < D / 64; ++a)
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4*>(mrow + a * (128 * 128) + cc * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(4, 128);
+        if (ct == 0) mbar_arrive(mt_ready);
+
+        auto recast = [&]() {
+            if (!has_row) return;
+#pragma unroll 1
+            for (int i0 = 0; i0 < D; i0 += 32) {
+                uint32_t x[32];
+                tmem_ld32(tmem + TM_M + lane_base + i0, x);
+                tmem_wait_ld();
+                store_bf16_row(i0, x);
+            }
+        };
+        bool ok = true;
+        int upd = 0;
+        const int n_upd = (n_agg > 0 ? 1 : 0) + n_main;
+        for (int u = 0; u < n_upd; ++u) {
+            ok = bar_and(4, 128, mbar_wait(upd_done, upd++ & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            if (u + 1 < n_upd) {
+                recast();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(4, 128);
+                if (ct == 0) mbar_arrive(mt_ready);
+            } else if (writes_state && p.M_out && has_row) {
+                float* dst = p.M_out + (int64_t)bh * D * DV + j;
+#pragma unroll 1
+                for (int i0 = 0; i0 < D; i0 += 32) {
+                    uint32_t x[32];
+                    tmem_ld32(tmem + TM_M + lane_base + i0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dst[(int64_t)(i0 + e) * DV] = __uint_as_float(x[e]);
+                }
+            }
+        }
+        if (!ok && ct == 0) record_timeout(p.status, abort_flag);
+    } else if (warp >= 8 && warp < 12) {
+        // ======================================================== E: out = O / den
+        const int ct = threadIdx.x - 256;
+        const int q = warp & 3;
+        const int j = 32 * q + lane;              // dv index
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const bool has_row = 32 * q < DV;
+        uint8_t* obase = sm + L::OT + (j >> 6) * ATOM + (j & 7) * 2;
+        const int cc = (j & 63) >> 3;
+        const uint64_t pol = l2_evict_first_policy();  // out is written once
+        bool ok = true;
+        for (int m = 0; m < n_main; ++m) {
+            const int buf = m & 1;
+            ok = bar_and(3, 128, mbar_wait(&o_full[buf], (m >> 1) & 1, abort_flag) &&
+                                     mbar_wait(&p_full[buf], (m >> 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            if (ct == 0) tma_store_wait_read0();  // previous out tile read by the TMA unit
+            named_bar_sync(3, 128);
+            if (has_row) {
+                const float* rd = rden + buf * 64;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t x[32];
+                    tmem_ld32(tmem + tm_o(buf) + lane_base + 32 * half, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int t = 32 * half + e;
+                        *reinterpret_cast<__nv_bfloat16*>(obase + t * 128 + ((cc ^ (t & 7)) << 4)) =
+                            __float2bfloat16_rn(__uint_as_float(x[e]) * rd[t]);
+                    }
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar_sync(3, 128);
+            if (ct == 0) {
+                mbar_arrive(&o_free[buf]);
+                const int t = (main_begin + m) * CH;
+#pragma unroll
+                for (int a = 0; a < DV / 64; ++a)
+                    tma_store_4d_hint(&mo, sm + L::OT + a * ATOM, a * 64, t, h, b, pol);
+                tma_store_commit();
+            }
+        }
+        if (!ok && ct == 0) record_timeout(p.status, abort_flag);
+        if (ct == 0) tma_store_wait_all0();
+    } else if (warp >= 12 && warp < 14) {
+        // ======================================================== S: P and 1/den
+        const int ct = threadIdx.x - 384;
+        const int q = warp & 3;                   // 0 or 1
+        const int t = 32 * q + lane;              // query row in the chunk
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        bool ok = true;
+        for (int m = 0; m < n_main; ++m) {
+            const int buf = m & 1;
+            bool w = mbar_wait(&s_full[buf], (m >> 1) & 1, abort_flag);
+            if (m >= 2) w = w && mbar_wait(&o_free[buf], ((m - 2) >> 1) & 1, abort_flag);  // rden[buf] consumed
+            ok = bar_and(2, 64, w);
+            if (!ok) break;
+            tc_fence_after();
+            uint8_t* prow = sm + L::PT + buf * ATOM + t * 128;
+            float rowsum = 0.f;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t x[32];
+                tmem_ld32(tmem + tm_s(buf) + lane_base + 32 * half, x);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int c0 = 32 * half + 2 * jj;
+                    const float s0 = (c0 <= t) ? __uint_as_float(x[2 * jj]) : 0.f;
+                    const float s1 = (c0 + 1 <= t) ? __uint_as_float(x[2 * jj + 1]) : 0.f;
+                    pk[jj] = pack_bf16(s0, s1);
+                    rowsum += bf16lo(pk[jj]) + bf16hi(pk[jj]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c2 = 4 * half + u;
+                    *reinterpret_cast<uint4*>(prow + ((c2 ^ (t & 7)) << 4)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+            }
+            uint32_t zc[16];
+            tmem_ld16(tmem + tm_s(buf) + lane_base + 64, zc);
+            tmem_wait_ld();
+            rden[buf * 64 + t] = 1.f / (__uint_as_float(zc[0]) + rowsum + p.eps);
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar_sync(2, 64);
+            if (ct == 0) {
+                mbar_arrive(&s_free[buf]);
+                mbar_arrive(&p_full[buf]);
+            }
+        }
+        if (!ok && ct == 0) record_timeout(p.status, abort_flag);
+    } else {
+        // ======================================================== F: phi and z (warps 2, 3, 14, 15)
+        const int ct = (warp == 2 ? 0 : warp == 3 ? 32 : warp == 14 ? 64 : 96) + lane;
+        if (ct < D) {
+            float zz = p.z_in ? p.z_in[(int64_t)bh * D + ct] : 0.f;
+            for (int pp = 0; pp < nws; ++pp) zz += agg[pp * p.rec + D * DV + ct];
+            zf[ct] = zz;
+        }
+        for (int idx = ct; idx < NST * (D / 64) * 15 * 8; idx += 128) {
+            const int c16 = idx % 8, row = 65 + (idx / 8) % 15, sa = idx / (8 * 15);
+            *reinterpret_cast<uint4*>(sm + L::K0 + sa * ATOMK + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+        }
+        named_bar_sync(1, 128);
+        bool ok = true;
+        for (int g = 0; g < nchunks; ++g) {
+            const int s = g % NST;
+            const bool is_main = g >= n_agg;
+            ok = bar_and(1, 128, mbar_wait(&full[s], (g / NST) & 1, abort_flag));
+            if (!ok) break;
+            uint8_t* qb = sm + L::Q0 + s * L::QB;
+            uint8_t* kb = sm + L::K0 + s * L::KB;
+            const int64_t t0 = (int64_t)(is_main ? main_begin + g - n_agg : g) * CH;
+            const int valid = (int)min64(CH, p.T - t0);
+            if (is_main && ct < D)  // row 64 (a multiple of 8: no swizzle offset) carries z before this chunk
+                *reinterpret_cast<__nv_bfloat16*>(kb + (ct >> 6) * ATOMK + 64 * 128 + (ct & 63) * 2) =
+                    __float2bfloat16_rn(zf[ct]);
+            float colsum[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) colsum[e] = 0.f;
+            if (is_main) phi_tile<D>(qb, ATOM, CH, ct, nullptr);
+            phi_tile<D>(kb, ATOMK, valid, ct, colsum);
+            float* zp = zpart + (g & 1) * 4 * D;
+            colsum_to_smem<D>(colsum, zp, ct);
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (ct == 0) mbar_arrive(&phib[s]);
+            if (ct < D) zf[ct] += zp[ct] + zp[D + ct] + zp[2 * D + ct] + zp[3 * D + ct];
+        }
+        if (!ok && ct == 0) record_timeout(p.status, abort_flag);
+        if (ok && writes_state && p.z_out && ct < D) p.z_out[(int64_t)bh * D + ct] = zf[ct];
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, int DV>
+static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
+    using L = FwdLayout<D, DV>;
+    static_assert(L::ALLOC <= 227 * 1024, "shared memory budget");
+    auto fn = fwd_tc_kernel<D, DV>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.nranges, B * p.H);
+    fn<<<grid, 512, L::ALLOC, s>>>(mq, mk, mv, mo, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
+    if (d == 128 && dv == 128) return launch_t<128, 128>(p, B, mq, mk, mv, mo, s);
+    if (d == 128 && dv == 64) return launch_t<128, 64>(p, B, mq, mk, mv, mo, s);
+    if (d == 64 && dv == 128) return launch_t<64, 128>(p, B, mq, mk, mv, mo, s);
+    if (d == 64 && dv == 64) return launch_t<64, 64>(p, B, mq, mk, mv, mo, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace la

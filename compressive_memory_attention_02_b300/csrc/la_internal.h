@@ -90,16 +90,21 @@ struct DecodeParams {
     float eps;
 };
 
-// Tensor-core forward: one block per (range, b*H + h).
+// Tensor-core forward: one block per (range, b*H + h). Range r processes the main
+// chunks [main_begin(r), main_end(r)); its start state is M_in (or zero) plus, in the
+// "parts" schedule, the aggregates of ranges 0..r-1 from parts_tc (records in ws),
+// or, in the "fused two-range" schedule, the aggregate of chunks [0, split) that
+// range 1 forms itself before its main chunks.
 struct FwdTcParams {
     const float* M_in;
     const float* z_in;
     float* M_out;
     float* z_out;
-    const float* ws;       // range aggregates from parts_tc (records of all ranges but the last)
+    const float* ws;       // parts schedule: records of ranges 0..nranges-2
     int64_t rec;           // floats per record (d*dv + d); M at +0, z at +d*dv
     int nranges;
-    int chunks_per_range;
+    int chunks_per_range;  // parts schedule
+    int split;             // fused schedule: first chunk of range 1 (0 = parts schedule)
     int H;
     int64_t T;
     float eps;

@@ -1,0 +1,102 @@
+// Helpers shared by the tensor-core kernels: tile geometry, bounded waits that
+// unwind consistently, and the in-place phi transform of a TMA-loaded tile.
+#pragma once
+#include "la_internal.h"
+
+namespace la {
+
+constexpr int CH = 64;                 // tokens per chunk on the tensor-core path
+constexpr int ATOM = 64 * 128;         // one 64-row, 128-byte-wide swizzle block column
+constexpr int KROWS = 80;              // forward K tile rows: 64 keys, z row, 15 zero rows
+constexpr int ATOMK = KROWS * 128;
+
+// Round the dynamic shared-memory base up to 1024 bytes (the 128-byte swizzle repeats
+// every 1024 bytes). Plain pointer arithmetic on the __shared__ array, so the compiler
+// still knows every derived pointer is a shared-memory address (ld/st.shared rather
+// than generic accesses).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// AND-reduce a predicate over the `n` threads of named barrier `id`.
+__device__ __forceinline__ bool bar_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {
+    *abort_flag = 1;
+    if (status) atomicOr(status, STATUS_TIMEOUT);
+}
+
+// Bounded wait that ignores the abort flag (used while draining at exit).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+    const unsigned long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > LA_WAIT_CYCLES) return false;
+    }
+    return true;
+}
+
+// phi in place on a [64 x D] bf16 tile (atoms `astride` bytes apart), by 128 threads.
+// Thread ct owns 16-byte chunk column j = ct % (D/8) of rows g, g + RG, ...
+// (g = ct / (D/8)); since RG is a multiple of 8 the swizzled chunk position
+// j ^ (row % 8) is the same for all of its rows. Rows >= valid become 0 (phi(0) = 1
+// must not enter the sums; pass valid = 64 to keep all rows). With colsum != nullptr
+// the thread adds the bf16-rounded results of its 8 columns into colsum[0..8).
+// Kept as a compact loop: this code runs beside other warp roles and must stay
+// resident in the instruction caches.
+template <int D>
+__device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, int ct, float* colsum) {
+    constexpr int CPR = D / 8;
+    constexpr int RG = 128 / CPR;
+    constexpr int RPT = CH / RG;
+    const int j = ct % CPR, g = ct / CPR;
+    uint8_t* base = tile + (j >> 3) * astride + (((j & 7) ^ (g & 7)) << 4) + g * 128;
+#pragma unroll 1
+    for (int i = 0; i < RPT; ++i) {
+        uint4* ptr = reinterpret_cast<uint4*>(base + i * RG * 128);
+        uint4 x = *ptr;
+        uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        const bool live = g + i * RG < valid;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float lo = phi_f(bf16lo(w[e])), hi = phi_f(bf16hi(w[e]));
+            w[e] = live ? pack_bf16(lo, hi) : 0u;
+        }
+        *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+        if (colsum) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                colsum[2 * e] += bf16lo(w[e]);
+                colsum[2 * e + 1] += bf16hi(w[e]);
+            }
+        }
+    }
+}
+
+// Combine the per-thread column sums of phi_tile into zpart[warp][D] (lanes that hold
+// a full warp's sum for chunk column j = lane write columns 8j..8j+7).
+template <int D>
+__device__ __forceinline__ void colsum_to_smem(float* colsum, float* zpart, int ct) {
+    constexpr int CPR = D / 8;
+#pragma unroll
+    for (int off = CPR; off < 32; off <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) colsum[e] += __shfl_xor_sync(0xffffffffu, colsum[e], off);
+    const int lane = ct & 31, w = ct >> 5;
+    if (lane < CPR)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zpart[w * D + lane * 8 + e] = colsum[e];
+}
+
+}  // namespace la
