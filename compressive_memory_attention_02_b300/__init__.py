@@ -17,10 +17,12 @@ LIB_PATH = os.path.join(_HERE, "liblinattn.so")
 
 LA_F32, LA_BF16 = 0, 1
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
+LA_ERR_SCRATCH_LIMIT = 6
+LA_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's static prefill scratch
 
 EXPORTS = (
     "la_causal_fwd", "la_causal_fwd_ex", "la_causal_fwd_workspace_size",
-    "la_prefill_state", "la_prefill_state_ex", "la_prefill_workspace_size",
+    "la_prefill_state", "la_prefill_state_ex", "la_prefill_workspace_size", "la_prefill_state_noalloc",
     "la_decode_step", "la_set_workspace", "la_get_last_device_status",
     "la_get_error_string", "la_last_launch_count",
 )
@@ -46,6 +48,7 @@ def _load() -> ctypes.CDLL:
     lib.la_causal_fwd_workspace_size.restype = sz
     lib.la_prefill_state.argtypes = fwd + [vp]
     lib.la_prefill_state_ex.argtypes = fwd + [i64p, vp, sz, vp]
+    lib.la_prefill_state_noalloc.argtypes = fwd + [vp]
     lib.la_prefill_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32]
     lib.la_prefill_workspace_size.restype = sz
     lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
@@ -142,6 +145,16 @@ def la_prefill_state_ex(q, k, v, out_last, M_in, z_in, M_out, z_out, B, H, T, d,
                                  _ptr(M_out), _ptr(z_out), B, H, T, d, dv, segment, eps, _dtype(dtype, q),
                                  _strides(strides), _ptr(workspace), int(workspace_bytes), _stream(stream, q))
     return _check("la_prefill_state_ex", rc)
+
+
+def la_prefill_state_noalloc(q, k, v, out_last, M_in, z_in, M_out, z_out, B, H, T, d, dv, segment, eps,
+                             dtype=None, stream=None):
+    """Prefill whose multi-part scratch is the library's own static device buffer
+    (LA_NOALLOC_SCRATCH_BYTES): nothing is allocated, by the library or here."""
+    rc = lib.la_prefill_state_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out_last), _ptr(M_in), _ptr(z_in),
+                                      _ptr(M_out), _ptr(z_out), B, H, T, d, dv, segment, eps, _dtype(dtype, q),
+                                      _stream(stream, q))
+    return _check("la_prefill_state_noalloc", rc)
 
 
 def la_prefill_workspace_size(B, H, T, d, dv, segment, dtype) -> int:

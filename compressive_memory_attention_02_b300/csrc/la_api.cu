@@ -279,7 +279,7 @@ static PrefillPlan plan_prefill(int B, int H, int64_t T, int d, int dv, int segm
     return pl;
 }
 
-static int prefill_impl(const void* q, const void* k, const void* v, void* out_last, const float* M_in,
+int prefill_impl(const void* q, const void* k, const void* v, void* out_last, const float* M_in,
                         const float* z_in, float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv,
                         int segment, float eps, la_dtype dtype, const int64_t* strides, void* ws, size_t ws_bytes,
                         bool use_registered, cudaStream_t stream) {
@@ -494,6 +494,7 @@ const char* la_get_error_string(int code) {
         case LA_ERR_CUDA: return "CUDA runtime or launch failure";
         case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
         case LA_ERR_WORKSPACE: return "workspace pointer not 256-byte aligned";
+        case LA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's static buffer holds";
         default: return "unknown error";
     }
 }

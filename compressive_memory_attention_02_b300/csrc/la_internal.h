@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/linattn.h"
 #include "la_ptx.cuh"
 
 namespace la {
@@ -128,5 +129,12 @@ cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_parts_tc(const PartsParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s);
+
+// Prefill behind la_prefill_state / la_prefill_state_ex (la_api.cu): with use_registered the
+// buffer given to la_set_workspace is the scratch, otherwise (ws, ws_bytes).
+int prefill_impl(const void* q, const void* k, const void* v, void* out_last, const float* M_in, const float* z_in,
+                 float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv, int segment, float eps,
+                 la_dtype dtype, const int64_t* strides, void* ws, size_t ws_bytes, bool use_registered,
+                 cudaStream_t stream);
 
 }  // namespace la

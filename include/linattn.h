@@ -60,7 +60,9 @@ enum {
     LA_ERR_UNSUPPORTED = 2,   /* d, dv, chunk or dtype outside the supported set */
     LA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
     LA_ERR_TIMEOUT = 4,       /* device status: a bounded wait inside a kernel ran out */
-    LA_ERR_WORKSPACE = 5      /* workspace pointer misaligned */
+    LA_ERR_WORKSPACE = 5,     /* workspace pointer misaligned */
+    LA_ERR_SCRATCH_LIMIT = 6  /* la_prefill_state_noalloc: the problem needs more scratch than
+                                 LA_NOALLOC_SCRATCH_BYTES */
 };
 
 /* ---- training forward (mode 3 of the mode table: all outputs) -------------
@@ -121,6 +123,35 @@ int la_prefill_state_ex(const void* q, const void* k, const void* v, void* out_l
 
 size_t la_prefill_workspace_size(int B, int H, int64_t T, int d, int dv, int segment,
                                  la_dtype dtype);
+
+/* ---- prefill without any device allocation ---------------------------------
+ * No counterpart on the method's pages: this entry point exists for callers that
+ * cannot allocate device memory at all. Examples are a host framework that hands an
+ * operator only its input and output buffers and owns every other byte of the GPU,
+ * and latency-critical code that may not call cudaMalloc because it can synchronise
+ * the device. Such callers cannot provide the workspace that la_prefill_state_ex
+ * takes, and la_prefill_state without a registered workspace falls back to the slow
+ * one-part schedule.
+ *
+ * Same arguments, results and layouts as la_prefill_state. The per-part sums go to a
+ * scratch array of LA_NOALLOC_SCRATCH_BYTES that lives inside the library as a
+ * statically sized device variable: every GPU that loads the library holds it until
+ * the process exits. The call allocates nothing and runs the same kernels as
+ * la_prefill_state_ex with a workspace of that size.
+ *   - Returns LA_ERR_SCRATCH_LIMIT, without launching, when
+ *     la_prefill_workspace_size(B, H, T, d, dv, segment, dtype) > LA_NOALLOC_SCRATCH_BYTES
+ *     (raise `segment` to use fewer parts; every part needs 4*(d*dv + d) bytes per head).
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents
+ *     (every byte a call reads it has written first). Calls whose executions overlap on
+ *     the GPU (different streams, not ordered) race on it: order them. */
+#define LA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int la_prefill_state_noalloc(const void* q, const void* k, const void* v, void* out_last,
+                             const float* M_in, const float* z_in, float* M_out, float* z_out,
+                             int B, int H, int64_t T, int d, int dv, int segment, float eps,
+                             la_dtype dtype, la_stream_t stream);
 
 /* ---- generation (pure sequential mode: one recurrent step) -----------------
  * For N independent streams x H heads, one token each:
