@@ -102,7 +102,8 @@ size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int 
 
 /* ---- prefill (prompt mode: state plus last output) ---------------------------
  * Only the final state and the last token's output, as the mode table's note
- * on the prompt mode says ("only S_n ... output in the last block"); the key-
+ * on the prompt mode says (the state alone, with the output formed in the last
+ * block); the key-
  * value sums are formed in parallel parts of `segment` tokens (the page's
  * remark that the sum can be done in parallel, e.g. as a tree) and added in
  * part order to M_in:  M_T = M_in + sum_p sum_{t in p} phi(k_t) v_t^T,
