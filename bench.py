@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-modes", action="store_true", help="skip the prefill and decode measurements")
     return ap.parse_args()
 
 
@@ -392,6 +393,92 @@ def report_ours(args, w, res, world):
     return line
 
 
+# ----------------------------------------------------------------------------- prefill and decode
+
+def _graph_time(call, reps, dev):
+    """Mean device time (ms) of one call: `reps` calls captured in one CUDA graph, replayed
+    once to warm up and once timed with CUDA events on the graph's stream."""
+    import torch
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            call()
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_modes(dev):
+    """The other two modes on their workloads: prefill (B=1 H=8 T=1,048,576, final state and
+    last output) and decode steps (256 streams x 32 heads). Kernel-only device time."""
+    import torch
+
+    import compressive_memory_attention_02_b300 as la
+    import synthetic
+    hbm_peak, _, src = peaks()
+    bf = lambda a: torch.from_numpy(a).view(torch.bfloat16).to(dev)
+    res = {}
+
+    w = synthetic.WORKLOADS["prefill"]
+    B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
+    k = bf(synthetic.normal(w.seed, synthetic.TID_K, (B, H, T, d), w.scale, "bf16"))
+    v = bf(synthetic.normal(w.seed, synthetic.TID_V, (B, H, T, dv), w.scale, "bf16"))
+    # only the last query token is read: the q tensor holds the recipe's values there
+    q = torch.empty_like(k)
+    for bh in range(B * H):
+        q.view(B * H, T, d)[bh, T - 1] = bf(synthetic.normal(w.seed, synthetic.TID_Q, (d,), w.scale, "bf16",
+                                                             first=(bh * T + T - 1) * d))
+    out = torch.empty(B, H, dv, dtype=torch.bfloat16, device=dev)
+    M = torch.empty(B, H, d, dv, device=dev)
+    z = torch.empty(B, H, d, device=dev)
+    nws = la.la_prefill_workspace_size(B, H, T, d, dv, w.segment, la.LA_BF16)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+    ms = _graph_time(lambda: la.la_prefill_state_ex(q, k, v, out, None, None, M, z, B, H, T, d, dv, w.segment,
+                                                    w.eps, la.LA_BF16, None, ws, nws), 5, dev)
+    assert la.la_get_last_device_status() == la.LA_OK
+    byt = B * H * T * (d + dv) * 2 + B * H * ((d * dv + d) * 4 + (d + dv) * 2)
+    res["prefill"] = {"workload": f"B={B} H={H} T={T} d=dv={d} bf16, parts of {w.segment}, final M,z + last output",
+                      "value": round(B * T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(ms, 4),
+                      "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
+                                   "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                                   "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs"}}
+    del q, k, v, ws
+
+    w = synthetic.WORKLOADS["generation"]
+    N, H, d, dv = w.B, w.H, w.d, w.dv
+    # the decode cost does not depend on the state's values: a seeded random state stands in
+    # for the 2048-token prompt's (the parity tests use the real prefill)
+    M = torch.from_numpy(synthetic.normal(w.seed, 7, (N, H, d, dv), 1.0, "f32")).to(dev)
+    z = torch.from_numpy(np.abs(synthetic.normal(w.seed, 8, (N, H, d), 1.0, "f32")) * 100 + 1000).to(dev)
+    toks = [tuple(bf(a) for a in synthetic.decode_tokens(w, s)) for s in range(8)]
+    out = torch.empty(N, H, dv, dtype=torch.bfloat16, device=dev)
+    step = [0]
+
+    def dec():
+        tq, tk, tv = toks[step[0] % len(toks)]
+        step[0] += 1
+        la.la_decode_step(tq, tk, tv, out, M, z, N, H, d, dv, w.eps, la.LA_BF16)
+    ms = _graph_time(dec, 64, dev)
+    assert la.la_get_last_device_status() == la.LA_OK
+    byt = N * H * (2 * (d * dv + d) * 4 + (2 * d + 2 * dv) * 2)
+    res["decode"] = {"workload": f"{N} streams x H={H}, d=dv={d}, bf16 tokens, fp32 state updated in place",
+                     "value": round(N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+                     "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
+                                  "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                                  "per_step_bytes": byt, "peak_source": f"{src} hbm_gbs"}}
+    return res
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -433,6 +520,9 @@ def main():
     res = run_ours(args, w, rank, world, dist)
     if rank == 0:
         line = report_ours(args, w, res, world)
+        if world == 1 and not args.no_modes:
+            import torch
+            line["modes"] = run_modes(torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
         if world == 1 and not args.no_cpu:
             hq, hk, hv = res["inputs"]
             tok, dt, threads, n = cpu_oracle_sample(w, hq, hk, hv, 0, budget_s=10.0)

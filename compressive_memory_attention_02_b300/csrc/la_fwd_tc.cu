@@ -8,20 +8,23 @@
 //     O^T = M_{c-1}^T phi(Q_c)^T + V_c^T P^T              dv x 64 (TMEM)
 //     out = O / den
 //     M^T += V_c^T phi(K_c) (f32 in TMEM),  z += colsum(phi(K_c)) (f32)
-// M^T is re-cast to bf16 in shared memory after every update, as the A operand of
-// the next chunk's inter-chunk MMA.
+// M^T is re-cast to bf16 after every update into a second TMEM region, which is the A
+// operand (read from tensor memory) of the next chunk's inter-chunk MMA; the state
+// never passes through shared memory.
 //
-// One block per (range, head). Warp roles (512 threads):
+// One block per (range, head). Warp roles (768 threads; warp w issues on sub-partition
+// w % 4 and may touch only TMEM lane quarter w % 4):
 //   warp 0        TMA producer: Q, K, V tiles into a 3-stage ring
-//   warp 1        TMEM owner; lane 0 issues every tcgen05.mma, software-pipelined
-//                 one chunk ahead: PV_c, then S'_{c+1}, inter_{c+1}, update_{c+1}
-//   warps 2,3,14,15  F: phi in place on Q and K, zero padded keys, column sums -> z
-//   warps 4-7     R: initial state into TMEM; bf16 re-cast of M after each update;
-//                 final M to global memory
-//   warps 8-11    E: out = O / den -> swizzled smem tile -> TMA store
-//   warps 12,13   S: P and 1/den from S'
-// A warp touches only its TMEM lane quarter (warp % 4). Each hand-off is an
-// mbarrier; TMEM reads and writes are ordered with tcgen05 fences around it.
+//   warp 1        TMEM owner; lane 0 issues every tcgen05.mma, software-pipelined one
+//                 chunk ahead: PV_c, then S'_{c+1}, inter_{c+1}, update_{c+1}
+//   warps 2,3,18-23  F: phi in place on Q and K, zero padded keys, column sums -> z
+//   warps 4-7     R: bf16 re-cast of M^T after each update; final M to global memory
+//   warps 8-15    E: initial state into TMEM; then out = O / den -> bf16, 8 x 8
+//                 transposes across lanes (O^T holds one feature per lane) -> swizzled
+//                 smem tile -> TMA store; warps 8-11 take tokens 0-31, 12-15 tokens 32-63
+//   warps 16,17   S: P and 1/den from S'
+// Each hand-off is an mbarrier; TMEM reads and writes are ordered with tcgen05 fences
+// around it.
 //
 // Sequence split: in the fused two-range schedule (split > 0) range 1 first forms
 // the state of chunks [0, split) itself (phi(K) and the update only) while range 0
@@ -32,10 +35,13 @@
 // r at chunk c ^ (r % 8)): Q, K, V tiles as TMA loads them ([64 tokens][64 features]
 // per atom; K atoms have 16 extra rows: row 64 holds bf16 z_{c-1}, rows 65-79 zero);
 // phi(Q), phi(K) read K-major for S' and inter; phi(K), V read MN-major (K = tokens)
-// for the update and PV; P [64 queries][64 keys] K-major; M^T bf16 [128][d] K-major.
+// for the update and PV; P [64 queries][64 keys] K-major.
 #include "la_tc_common.cuh"
 
 namespace la {
+
+constexpr int FWD_THREADS = 768;
+constexpr int NFW = 8;  // F warps
 
 template <int D, int DV>
 struct FwdLayout {
@@ -46,15 +52,12 @@ struct FwdLayout {
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + NST * QB;     // an M=128 read past the last Q atom lands here
     static constexpr int V0 = K0 + NST * KB;
-    static constexpr int MT = V0 + NST * VB;     // an M=128 read past a 64-wide V tile lands here
-    static constexpr int MTB = D / 64 * (128 * 128);
-    static constexpr int PT = MT + MTB;          // P, two buffers
+    static constexpr int PT = V0 + NST * VB;     // P, two buffers; an M=128 read past a 64-wide V tile lands here
     static constexpr int OT = PT + 2 * ATOM;     // out tile
-    static constexpr int SMALL = OT + DV / 64 * ATOM;
-    static constexpr int RDEN = SMALL;           // 2 x 64 floats
-    static constexpr int ZF = RDEN + 2 * 64 * 4;  // 128 floats
-    static constexpr int ZP = ZF + 128 * 4;      // 2 x 4 x D floats
-    static constexpr int BAR = ZP + 2 * 4 * D * 4;
+    static constexpr int RDEN = OT + DV / 64 * ATOM;  // 2 x 64 floats
+    static constexpr int ZF = RDEN + 2 * 64 * 4;      // 128 floats
+    static constexpr int ZP = ZF + 128 * 4;           // 2 x NFW x D floats
+    static constexpr int BAR = ZP + 2 * NFW * D * 4;
     static constexpr int NBAR = 22;
     static constexpr int MISC = BAR + 8 * NBAR;
     static constexpr int TOTAL = MISC + 16;
@@ -62,12 +65,19 @@ struct FwdLayout {
 };
 
 // TMEM column map (512 columns allocated)
-constexpr uint32_t TM_M = 0;                                                      // M^T f32, d columns
-__device__ __forceinline__ uint32_t tm_s(int buf) { return 128u + 80u * buf; }  // S', 80 columns each
-__device__ __forceinline__ uint32_t tm_o(int buf) { return 288u + 64u * buf; }  // O^T, 64 columns each
+constexpr uint32_t TM_M = 0;     // M^T f32, d columns
+constexpr uint32_t TM_A = 128;   // M^T bf16, two per column: d/2 columns (A operand of inter)
+__device__ __forceinline__ uint32_t tm_s(int buf) { return 192u + 80u * buf; }  // S', 80 columns each
+__device__ __forceinline__ uint32_t tm_o(int buf) { return 352u + 64u * buf; }  // O^T, 64 columns each
+
+// 32 f32 values -> 16 words of two bf16 (low half = even index)
+__device__ __forceinline__ void pack32_bf16(const uint32_t* x, uint32_t* a) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) a[k] = pack_bf16(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1]));
+}
 
 template <int D, int DV>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, FwdTcParams p) {
     using L = FwdLayout<D, DV>;
@@ -164,7 +174,7 @@ __global__ void __launch_bounds__(512, 1)
             constexpr uint32_t id_pv = idesc_bf16(128, CH, 1, 0);    // O^T += V^T P^T
             constexpr uint32_t id_in = idesc_bf16(128, CH, 0, 0);    // O^T = M^T phiQ^T
             const uint32_t q0 = smem_u32(sm + L::Q0), k0 = smem_u32(sm + L::K0), v0 = smem_u32(sm + L::V0);
-            const uint32_t mt = smem_u32(sm + L::MT), pt = smem_u32(sm + L::PT);
+            const uint32_t pt = smem_u32(sm + L::PT);
             bool ok = true;
             int mt_waits = 0;
             auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -201,8 +211,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks & 3) * 32;
-                    mma_bf16_ss(tmem + tm_o(buf), sdesc_sw128(mt + (ks >> 2) * (128 * 128) + off, 16, 1024),
-                                sdesc_sw128(qb + (ks >> 2) * ATOM + off, 16, 1024), id_in, ks != 0);
+                    mma_bf16_ts(tmem + tm_o(buf), tmem + TM_A + ks * 8, sdesc_sw128(qb + (ks >> 2) * ATOM + off, 16, 1024),
+                                id_in, ks != 0);
                 }
                 update(s);
                 mma_commit(upd_done);
@@ -237,61 +247,23 @@ __global__ void __launch_bounds__(512, 1)
             mbar_wait_drain(drain, 0);
         }
     } else if (warp >= 4 && warp < 8) {
-        // ======================================================== R: state
+        // ======================================================== R: state re-cast
         const int ct = threadIdx.x - 128;
         const int q = warp & 3;
         const int j = 32 * q + lane;              // dv row of M^T
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const bool has_row = 32 * q < DV;         // warp-uniform
-        uint8_t* mrow = sm + L::MT + j * 128;
-        auto store_bf16_row = [&](int i0, const uint32_t* x) {  // 32 f32 values, columns i0..i0+31
-            uint8_t* atom = mrow + (i0 >> 6) * (128 * 128);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int cc = ((i0 & 63) >> 3) + u;
-                const uint32_t* y = x + 8 * u;
-                *reinterpret_cast<uint4*>(atom + ((cc ^ (j & 7)) << 4)) =
-                    make_uint4(pack_bf16(__uint_as_float(y[0]), __uint_as_float(y[1])),
-                               pack_bf16(__uint_as_float(y[2]), __uint_as_float(y[3])),
-                               pack_bf16(__uint_as_float(y[4]), __uint_as_float(y[5])),
-                               pack_bf16(__uint_as_float(y[6]), __uint_as_float(y[7])));
-            }
-        };
-        if (has_row) {
-#pragma unroll 1
-            for (int i0 = 0; i0 < D; i0 += 32) {
-                uint32_t x[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int i = i0 + e;
-                    float m = p.M_in ? __ldg(p.M_in + ((int64_t)bh * D + i) * DV + j) : 0.f;
-                    for (int pp = 0; pp < nws; ++pp) m += __ldg(agg + pp * p.rec + i * DV + j);
-                    x[e] = __float_as_uint(m);
-                }
-                tmem_st16(tmem + TM_M + lane_base + i0, x);
-                tmem_st16(tmem + TM_M + lane_base + i0 + 16, x + 16);
-                store_bf16_row(i0, x);
-            }
-            tmem_wait_st();
-        } else {
-            for (int a = 0; a < D / 64; ++a)
-                for (int cc = 0; cc < 8; ++cc)
-                    *reinterpret_cast<uint4*>(mrow + a * (128 * 128) + cc * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(4, 128);
-        if (ct == 0) mbar_arrive(mt_ready);
-
         auto recast = [&]() {
             if (!has_row) return;
 #pragma unroll 1
             for (int i0 = 0; i0 < D; i0 += 32) {
-                uint32_t x[32];
+                uint32_t x[32], a[16];
                 tmem_ld32(tmem + TM_M + lane_base + i0, x);
                 tmem_wait_ld();
-                store_bf16_row(i0, x);
+                pack32_bf16(x, a);
+                tmem_st16(tmem + TM_A + lane_base + i0 / 2, a);
             }
+            tmem_wait_st();
         };
         bool ok = true;
         int upd = 0;
@@ -302,7 +274,6 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after();
             if (u + 1 < n_upd) {
                 recast();
-                fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(4, 128);
                 if (ct == 0) mbar_arrive(mt_ready);
@@ -319,43 +290,78 @@ __global__ void __launch_bounds__(512, 1)
             }
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
-    } else if (warp >= 8 && warp < 12) {
-        // ======================================================== E: out = O / den
+    } else if (warp >= 8 && warp < 16) {
+        // ======================================================== E: initial state, then out = O / den
         const int ct = threadIdx.x - 256;
         const int q = warp & 3;
-        const int j = 32 * q + lane;              // dv index
+        const int hf = (warp - 8) >> 2;           // rows 64hf.. of the initial state; tokens 32hf.. of a chunk
+        const int j = 32 * q + lane;              // dv index: row of O^T and of M^T
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const bool has_row = 32 * q < DV;
-        uint8_t* obase = sm + L::OT + (j >> 6) * ATOM + (j & 7) * 2;
-        const int cc = (j & 63) >> 3;
+        const bool has_row = 32 * q < DV;         // warp-uniform
+        if (has_row) {
+            // column j of the initial state M_in (+ range aggregates), rows [64hf, 64hf + 64)
+            const float* src = p.M_in ? p.M_in + (int64_t)bh * D * DV + j : nullptr;
+#pragma unroll 1
+            for (int i0 = 64 * hf; i0 < D && i0 < 64 * hf + 64; i0 += 32) {
+                uint32_t x[32], a[16];
+                if (src) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__ldg(src + (int64_t)(i0 + e) * DV));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = 0u;
+                }
+#pragma unroll 1
+                for (int pp = 0; pp < nws; ++pp) {
+                    const float* ag = agg + pp * p.rec + (int64_t)i0 * DV + j;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) + __ldg(ag + e * DV));
+                }
+                tmem_st16(tmem + TM_M + lane_base + i0, x);
+                tmem_st16(tmem + TM_M + lane_base + i0 + 16, x + 16);
+                pack32_bf16(x, a);
+                tmem_st16(tmem + TM_A + lane_base + i0 / 2, a);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        named_bar_sync(3, 256);
+        if (ct == 0) mbar_arrive(mt_ready);
+
+        // Lane l holds feature j of the chunk's outputs. After an 8 x 8 transpose within its
+        // group of 8 lanes it holds token t (t % 8 == l % 8) of the features j0 .. j0+7,
+        // j0 = 32q + 8(l / 8): one 16-byte chunk of the [token][feature] tile.
+        const int i8 = lane & 7;
+        const int j0 = 32 * q + (lane & ~7);
+        uint8_t* obase = sm + L::OT + (j0 >> 6) * ATOM + ((((j0 & 63) >> 3) ^ i8) << 4);
         const uint64_t pol = l2_evict_first_policy();  // out is written once
         bool ok = true;
         for (int m = 0; m < n_main; ++m) {
             const int buf = m & 1;
-            ok = bar_and(3, 128, mbar_wait(&o_full[buf], (m >> 1) & 1, abort_flag) &&
+            ok = bar_and(3, 256, mbar_wait(&o_full[buf], (m >> 1) & 1, abort_flag) &&
                                      mbar_wait(&p_full[buf], (m >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             if (ct == 0) tma_store_wait_read0();  // previous out tile read by the TMA unit
-            named_bar_sync(3, 128);
+            named_bar_sync(3, 256);
             if (has_row) {
-                const float* rd = rden + buf * 64;
+                const float4* rd4 = reinterpret_cast<const float4*>(rden + buf * 64);
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t x[32];
-                    tmem_ld32(tmem + tm_o(buf) + lane_base + 32 * half, x);
+                for (int bb = 4 * hf; bb < 4 * hf + 4; ++bb) {  // tokens 8bb .. 8bb+7 (compact: see phi_tile)
+                    uint32_t x[8];
+                    tmem_ld8(tmem + tm_o(buf) + lane_base + 8 * bb, x);
+                    const float4 ra = rd4[2 * bb], rb = rd4[2 * bb + 1];
                     tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int t = 32 * half + e;
-                        *reinterpret_cast<__nv_bfloat16*>(obase + t * 128 + ((cc ^ (t & 7)) << 4)) =
-                            __float2bfloat16_rn(__uint_as_float(x[e]) * rd[t]);
-                    }
+                    const float* xs = reinterpret_cast<const float*>(x);
+                    uint32_t w[4] = {pack_bf16(xs[0] * ra.x, xs[1] * ra.y), pack_bf16(xs[2] * ra.z, xs[3] * ra.w),
+                                     pack_bf16(xs[4] * rb.x, xs[5] * rb.y), pack_bf16(xs[6] * rb.z, xs[7] * rb.w)};
+                    transpose8x8_b16(w, lane);
+                    *reinterpret_cast<uint4*>(obase + (8 * bb + i8) * 128) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            named_bar_sync(3, 128);
+            named_bar_sync(3, 256);
             if (ct == 0) {
                 mbar_arrive(&o_free[buf]);
                 const int t = (main_begin + m) * CH;
@@ -367,9 +373,9 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
         if (ct == 0) tma_store_wait_all0();
-    } else if (warp >= 12 && warp < 14) {
+    } else if (warp >= 16 && warp < 18) {
         // ======================================================== S: P and 1/den
-        const int ct = threadIdx.x - 384;
+        const int ct = threadIdx.x - 512;
         const int q = warp & 3;                   // 0 or 1
         const int t = 32 * q + lane;              // query row in the chunk
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
@@ -418,23 +424,23 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
     } else {
-        // ======================================================== F: phi and z (warps 2, 3, 14, 15)
-        const int ct = (warp == 2 ? 0 : warp == 3 ? 32 : warp == 14 ? 64 : 96) + lane;
+        // ======================================================== F: phi and z (warps 2, 3, 18-23)
+        const int ct = (warp < 4 ? warp - 2 : warp - 16) * 32 + lane;
         if (ct < D) {
             float zz = p.z_in ? p.z_in[(int64_t)bh * D + ct] : 0.f;
             for (int pp = 0; pp < nws; ++pp) zz += agg[pp * p.rec + D * DV + ct];
             zf[ct] = zz;
         }
-        for (int idx = ct; idx < NST * (D / 64) * 15 * 8; idx += 128) {
+        for (int idx = ct; idx < NST * (D / 64) * 15 * 8; idx += 32 * NFW) {
             const int c16 = idx % 8, row = 65 + (idx / 8) % 15, sa = idx / (8 * 15);
             *reinterpret_cast<uint4*>(sm + L::K0 + sa * ATOMK + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 32 * NFW);
         bool ok = true;
         for (int g = 0; g < nchunks; ++g) {
             const int s = g % NST;
             const bool is_main = g >= n_agg;
-            ok = bar_and(1, 128, mbar_wait(&full[s], (g / NST) & 1, abort_flag));
+            ok = bar_and(1, 32 * NFW, mbar_wait(&full[s], (g / NST) & 1, abort_flag));
             if (!ok) break;
             uint8_t* qb = sm + L::Q0 + s * L::QB;
             uint8_t* kb = sm + L::K0 + s * L::KB;
@@ -446,14 +452,19 @@ __global__ void __launch_bounds__(512, 1)
             float colsum[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) colsum[e] = 0.f;
-            if (is_main) phi_tile<D>(qb, ATOM, CH, ct, nullptr);
-            phi_tile<D>(kb, ATOMK, valid, ct, colsum);
-            float* zp = zpart + (g & 1) * 4 * D;
+            if (is_main) phi_tile<D, 32 * NFW>(qb, ATOM, CH, ct, nullptr);
+            phi_tile<D, 32 * NFW>(kb, ATOMK, valid, ct, colsum);
+            float* zp = zpart + (g & 1) * NFW * D;
             colsum_to_smem<D>(colsum, zp, ct);
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
+            named_bar_sync(1, 32 * NFW);
             if (ct == 0) mbar_arrive(&phib[s]);
-            if (ct < D) zf[ct] += zp[ct] + zp[D + ct] + zp[2 * D + ct] + zp[3 * D + ct];
+            if (ct < D) {
+                float zz = zf[ct];
+#pragma unroll
+                for (int w = 0; w < NFW; ++w) zz += zp[w * D + ct];
+                zf[ct] = zz;
+            }
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
         if (ok && writes_state && p.z_out && ct < D) p.z_out[(int64_t)bh * D + ct] = zf[ct];
@@ -476,7 +487,7 @@ static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, 
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     dim3 grid(p.nranges, B * p.H);
-    fn<<<grid, 512, L::ALLOC, s>>>(mq, mk, mv, mo, p);
+    fn<<<grid, FWD_THREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
 }
 

@@ -47,33 +47,72 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     return true;
 }
 
-// phi in place on a [64 x D] bf16 tile (atoms `astride` bytes apart), by 128 threads.
+// phi on two packed bf16 values: exp(min(x, 0)) in f32 rounded to bf16, plus max(x, 0) in
+// bf16. For x <= 0 that is the rounded exponential; for x > 0 the exponential is exactly
+// 1 and the bf16 add rounds 1 + x once, so the result equals rounding the f32 value
+// exp(min(x, 0)) + max(x, 0) to bf16.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w);
+    const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+    const __nv_bfloat162 mn = __hmin2(x, zero);
+    const uint32_t m = *reinterpret_cast<const uint32_t*>(&mn);
+    constexpr float kLog2e = 1.4426950408889634f;
+    const __nv_bfloat162 e = __floats2bfloat162_rn(ex2_approx(bf16lo(m) * kLog2e), ex2_approx(bf16hi(m) * kLog2e));
+    const __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Transpose an 8 x 8 matrix of 16-bit values held by 8 consecutive lanes (lane i of the
+// group holds row i as four words of two values, low half first) so that lane i ends
+// up with column i. Three exchange steps over lane distances 4, 2, 1 swap blocks of
+// 4 x 4, 2 x 2 and single elements.
+__device__ __forceinline__ void transpose8x8_b16(uint32_t (&r)[4], int lane) {
+    const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+    uint32_t s0 = b2 ? r[0] : r[2], s1 = b2 ? r[1] : r[3];
+    s0 = __shfl_xor_sync(0xffffffffu, s0, 4);
+    s1 = __shfl_xor_sync(0xffffffffu, s1, 4);
+    if (b2) r[0] = s0, r[1] = s1;
+    else r[2] = s0, r[3] = s1;
+    s0 = b1 ? r[0] : r[1];
+    s1 = b1 ? r[2] : r[3];
+    s0 = __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+    if (b1) r[0] = s0, r[2] = s1;
+    else r[1] = s0, r[3] = s1;
+    const uint32_t sel_send = b0 ? 0x5410u : 0x7632u;  // even lanes send their high halves, odd the low
+    s0 = __shfl_xor_sync(0xffffffffu, __byte_perm(r[0], r[1], sel_send), 1);
+    s1 = __shfl_xor_sync(0xffffffffu, __byte_perm(r[2], r[3], sel_send), 1);
+    const uint32_t sa = b0 ? 0x3254u : 0x5410u, sb = b0 ? 0x3276u : 0x7610u;
+    r[0] = __byte_perm(r[0], s0, sa);
+    r[1] = __byte_perm(r[1], s0, sb);
+    r[2] = __byte_perm(r[2], s1, sa);
+    r[3] = __byte_perm(r[3], s1, sb);
+}
+
+// phi in place on a [64 x D] bf16 tile (atoms `astride` bytes apart), by NT threads.
 // Thread ct owns 16-byte chunk column j = ct % (D/8) of rows g, g + RG, ...
 // (g = ct / (D/8)); since RG is a multiple of 8 the swizzled chunk position
 // j ^ (row % 8) is the same for all of its rows. Rows >= valid become 0 (phi(0) = 1
 // must not enter the sums; pass valid = 64 to keep all rows). With colsum != nullptr
 // the thread adds the bf16-rounded results of its 8 columns into colsum[0..8).
-// Kept as a compact loop: this code runs beside other warp roles and must stay
-// resident in the instruction caches.
-template <int D>
+// Kept as a compact loop: this code runs beside other warp roles on the same
+// sub-partitions and must stay resident in the instruction caches.
+template <int D, int NT = 128>
 __device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, int ct, float* colsum) {
     constexpr int CPR = D / 8;
-    constexpr int RG = 128 / CPR;
+    constexpr int RG = NT / CPR;
+    static_assert(RG % 8 == 0 && CH % RG == 0, "rows of a thread share one swizzle phase");
     constexpr int RPT = CH / RG;
     const int j = ct % CPR, g = ct / CPR;
-    uint8_t* base = tile + (j >> 3) * astride + (((j & 7) ^ (g & 7)) << 4) + g * 128;
+    uint4* base = reinterpret_cast<uint4*>(tile + (j >> 3) * astride + (((j & 7) ^ (g & 7)) << 4) + g * 128);
 #pragma unroll 1
     for (int i = 0; i < RPT; ++i) {
-        uint4* ptr = reinterpret_cast<uint4*>(base + i * RG * 128);
-        uint4 x = *ptr;
+        uint4 x = base[i * RG * 8];
         uint32_t w[4] = {x.x, x.y, x.z, x.w};
         const bool live = g + i * RG < valid;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float lo = phi_f(bf16lo(w[e])), hi = phi_f(bf16hi(w[e]));
-            w[e] = live ? pack_bf16(lo, hi) : 0u;
-        }
-        *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 4; ++e) w[e] = live ? phi_bf16x2(w[e]) : 0u;
+        base[i * RG * 8] = make_uint4(w[0], w[1], w[2], w[3]);
         if (colsum) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
