@@ -180,10 +180,32 @@ def segment_major(a, S):
     return np.ascontiguousarray(a.reshape(B, H, S, T // S, x).transpose(2, 0, 1, 3, 4))
 
 
+def replica_seed(w, rank):
+    """Each rank runs its own replica of the workload (independent problems, weak
+    scaling): same recipe, a seed of its own."""
+    return w.seed + 7919 * rank
+
+
+def max_over_ranks(x, dist, device):
+    """Maximum of a per-rank float over all ranks (the slowest rank sets the time);
+    `device` is where the backend reduces (a CUDA device for NCCL, CPU for gloo)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(tokens_per_rank, seconds_max, world):
+    """Whole-job throughput: the tokens every rank processed over the slowest rank's time."""
+    return world * tokens_per_rank / seconds_max
+
+
 def make_inputs(w, rank):
     import synthetic
     S = w.T // w.segment
-    seed = w.seed + 7919 * rank
+    seed = replica_seed(w, rank)
     q = synthetic.normal(seed, synthetic.TID_Q, (w.B, w.H, w.T, w.d), w.scale, w.dtype)
     k = synthetic.normal(seed, synthetic.TID_K, (w.B, w.H, w.T, w.d), w.scale, w.dtype)
     v = synthetic.normal(seed, synthetic.TID_V, (w.B, w.H, w.T, w.dv), w.scale, w.dtype)
@@ -288,11 +310,7 @@ def run_ours(args, w, rank, world, dist):
     status = la.la_get_last_device_status()
     call_ms = [call_events[i][s].elapsed_time(call_events[i][s + 1]) for i in range(K) for s in range(S)]
 
-    if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([ms_total], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
 
     res = {"ms_total": ms_total, "call_ms": call_ms, "launches": launches_per_step * K, "status": status,
            "clocks": sampler.summary()}
@@ -342,11 +360,7 @@ def run_ours(args, w, rank, world, dist):
         for _ in range(Ke):
             e2e_step()
         e2e_s = time.perf_counter() - t0
-        if dist is not None:
-            import torch.distributed as tdist
-            t = torch.tensor([e2e_s], device=dev)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(e2e_s, dist, dev)
         res["e2e"] = {"steps": Ke, "seconds": e2e_s,
                       "h2d": int(sum(a.numel() * a.element_size() for a in (pq, pk, pv))),
                       "d2h": int(po.numel() * po.element_size() + pM.numel() * 4 + pz.numel() * 4)}
@@ -359,7 +373,7 @@ def report_ours(args, w, res, world):
     K = args.steps
     tokens_step = w.B * w.T
     ms_step = res["ms_total"] / K
-    value = world * tokens_step / (res["ms_total"] / 1e3 / K)
+    value = aggregate_rate(tokens_step, res["ms_total"] / 1e3 / K, world)
     bytes_step, flops_step = algorithmic(w)
     S = w.T // w.segment
     call_mean_ms = statistics.mean(res["call_ms"])
@@ -386,7 +400,7 @@ def report_ours(args, w, res, world):
     }
     if "e2e" in res:
         e = res["e2e"]
-        line["e2e"] = {"value": round(world * tokens_step * e["steps"] / e["seconds"], 1), "unit": UNIT,
+        line["e2e"] = {"value": round(aggregate_rate(tokens_step * e["steps"], e["seconds"], world), 1), "unit": UNIT,
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if res["status"] != 0:
         line["device_status"] = res["status"]

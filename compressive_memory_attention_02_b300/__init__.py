@@ -24,7 +24,7 @@ EXPORTS = (
     "la_causal_fwd", "la_causal_fwd_ex", "la_causal_fwd_workspace_size",
     "la_prefill_state", "la_prefill_state_ex", "la_prefill_workspace_size", "la_prefill_state_noalloc",
     "la_decode_step", "la_set_workspace", "la_get_last_device_status",
-    "la_get_error_string", "la_last_launch_count",
+    "la_get_error_string", "la_last_launch_count", "la_selftest_wait_timeout",
 )
 
 
@@ -57,6 +57,7 @@ def _load() -> ctypes.CDLL:
     lib.la_get_error_string.argtypes = [i32]
     lib.la_get_error_string.restype = ctypes.c_char_p
     lib.la_last_launch_count.argtypes = []
+    lib.la_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
     for name in EXPORTS:
         f = getattr(lib, name)
         if f.restype is ctypes.c_int or f.restype is None:
@@ -177,6 +178,11 @@ def la_get_last_device_status(stream=None) -> int:
 
 def la_get_error_string(code: int) -> str:
     return error_string(code)
+
+
+def la_selftest_wait_timeout(limit_cycles, stream=None):
+    return _check("la_selftest_wait_timeout",
+                  lib.la_selftest_wait_timeout(int(limit_cycles), _stream(stream) if stream is not None else None))
 
 
 def la_last_launch_count() -> int:

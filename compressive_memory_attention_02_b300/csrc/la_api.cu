@@ -44,6 +44,13 @@ static int current_device(DeviceState** st) {
     return LA_OK;
 }
 
+int device_status_word(int** status) {
+    DeviceState* ds = nullptr;
+    const int rc = current_device(&ds);
+    if (rc == LA_OK) *status = ds->status;
+    return rc;
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;

@@ -173,8 +173,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             constexpr uint32_t id_u = idesc_bf16(128, D, 1, 1);      // M^T += V^T phiK
             constexpr uint32_t id_pv = idesc_bf16(128, CH, 1, 0);    // O^T += V^T P^T
             constexpr uint32_t id_in = idesc_bf16(128, CH, 0, 0);    // O^T = M^T phiQ^T
-            const uint32_t q0 = smem_u32(sm + L::Q0), k0 = smem_u32(sm + L::K0), v0 = smem_u32(sm + L::V0);
-            const uint32_t pt = smem_u32(sm + L::PT);
+            // Descriptors of stage 0 / buffer 0; others differ only in the start-address field
+            // (bits 0-13, address >> 4), which stays below 2^14 for any shared-memory address,
+            // so an offset is added to the descriptor directly.
+            const uint64_t dq0 = sdesc_sw128(smem_u32(sm + L::Q0), 16, 1024);     // phiQ, K-major
+            const uint64_t dk0 = sdesc_sw128(smem_u32(sm + L::K0), 16, 1024);     // [phiK; z], K-major
+            const uint64_t dku0 = sdesc_sw128(smem_u32(sm + L::K0), ATOMK, 1024); // phiK, MN-major
+            const uint64_t dv0 = sdesc_sw128(smem_u32(sm + L::V0), ATOM, 1024);   // V, MN-major
+            const uint64_t dp0 = sdesc_sw128(smem_u32(sm + L::PT), 16, 1024);     // P, K-major
+            auto off = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
             bool ok = true;
             int mt_waits = 0;
             auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -185,35 +192,30 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 return ok;
             };
             auto update = [&](int s) {
-                const uint32_t vb = v0 + s * L::VB, kb = k0 + s * L::KB;
+                const uint64_t va = dv0 + off(s * L::VB), kb = dku0 + off(s * L::KB);
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks)
-                    mma_bf16_ss(tmem + TM_M, sdesc_sw128(vb + ks * 2048, ATOM, 1024),
-                                sdesc_sw128(kb + ks * 2048, ATOMK, 1024), id_u, 1);
+                    mma_bf16_ss(tmem + TM_M, va + off(ks * 2048), kb + off(ks * 2048), id_u, 1);
             };
             // S'_m, inter_m, update_m of main chunk m
             auto front = [&](int m) {
                 const int g = n_agg + m, s = g % NST, buf = m & 1;
-                const uint32_t qb = q0 + s * L::QB, kb = k0 + s * L::KB;
+                const uint64_t qd = dq0 + off(s * L::QB), kd = dk0 + off(s * L::KB);
                 if (!wait(&phib[s], (g / NST) & 1)) return false;
                 if (m >= 2 && !wait(&s_free[buf], ((m >> 1) - 1) & 1)) return false;
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks & 3) * 32;
-                    mma_bf16_ss(tmem + tm_s(buf), sdesc_sw128(qb + (ks >> 2) * ATOM + off, 16, 1024),
-                                sdesc_sw128(kb + (ks >> 2) * ATOMK + off, 16, 1024), id_s, ks != 0);
-                }
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_bf16_ss(tmem + tm_s(buf), qd + off((ks >> 2) * ATOM + (ks & 3) * 32),
+                                kd + off((ks >> 2) * ATOMK + (ks & 3) * 32), id_s, ks != 0);
                 mma_commit(&s_full[buf]);
                 if (!wait(mt_ready, mt_waits++ & 1)) return false;
                 if (m >= 2 && !wait(&o_free[buf], ((m >> 1) - 1) & 1)) return false;
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks & 3) * 32;
-                    mma_bf16_ts(tmem + tm_o(buf), tmem + TM_A + ks * 8, sdesc_sw128(qb + (ks >> 2) * ATOM + off, 16, 1024),
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_bf16_ts(tmem + tm_o(buf), tmem + TM_A + ks * 8, qd + off((ks >> 2) * ATOM + (ks & 3) * 32),
                                 id_in, ks != 0);
-                }
                 update(s);
                 mma_commit(upd_done);
                 return true;
@@ -237,8 +239,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks)
-                    mma_bf16_ss(tmem + tm_o(buf), sdesc_sw128(v0 + s * L::VB + ks * 2048, ATOM, 1024),
-                                sdesc_sw128(pt + buf * ATOM + ks * 32, 16, 1024), id_pv, 1);
+                    mma_bf16_ss(tmem + tm_o(buf), dv0 + off(s * L::VB + ks * 2048), dp0 + off(buf * ATOM + ks * 32),
+                                id_pv, 1);
                 mma_commit(&o_full[buf]);
                 mma_commit(&empty[s]);
                 if (m + 1 < n_main && !front(m + 1)) break;

@@ -130,6 +130,9 @@ cudaError_t launch_parts_tc(const PartsParams& p, const CUtensorMap& mk, const C
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s);
 
+// Device address of the current device's status word (la_api.cu).
+int device_status_word(int** status);
+
 // Prefill behind la_prefill_state / la_prefill_state_ex (la_api.cu): with use_registered the
 // buffer given to la_set_workspace is the scratch, otherwise (ws, ws_bytes).
 int prefill_impl(const void* q, const void* k, const void* v, void* out_last, const float* M_in, const float* z_in,

@@ -264,50 +264,62 @@ __global__ void __launch_bounds__(128) prefill_out_kernel(PrefillOutParams p) {
 }
 
 // ------------------------------------------------------------------ decode step
-// grid N*H, block 256. Thread (rg, cg) owns the float4 column group cg of rows
-// rg, rg + R, ... (R = 256 / (dv/4)); a warp covers 512 contiguous bytes of a row,
-// so every load and store of M is a coalesced 128-bit access. All of a thread's
-// rows are loaded before any is used, to keep many loads in flight.
+// grid (N*H, ceil(dv/64)), block 256, three blocks per SM. Block (nh, c) updates
+// columns [64c, 64c + 64) of M for every row and writes those outputs; it forms the
+// full denominator phi(q).(z + phi(k)) itself, and block c = 0 writes z back.
+// Thread (rg, cg) owns the float4 column group cg of rows rg, rg + R, ...
+// (R = 256 / (width/4), at most 8 rows); a warp covers 256 contiguous bytes of two
+// rows, so every load and store of M is a coalesced 128-bit access. The thread's rows
+// of M are requested first, before q, k, v and z, so the state stream does not wait
+// for the token's round trip; all of them are in flight before any is used.
+constexpr int DEC_NT = 256;
+constexpr int DEC_CW = 64;  // columns per block
+
 template <typename TI>
-__global__ void __launch_bounds__(256) decode_kernel(DecodeParams p) {
-    constexpr int MAXR = 16;
+__global__ void __launch_bounds__(DEC_NT, 3) decode_kernel(DecodeParams p) {
+    constexpr int MAXR = 8;  // d * DEC_CW / (4 * DEC_NT) rows per thread at d = 128
     __shared__ float fq[128], fk[128];
     __shared__ __align__(16) float vv[128];
-    __shared__ float4 red[256];
-    __shared__ float dred[8];
+    __shared__ float4 red[DEC_NT];
+    __shared__ float dred[DEC_NT / 32];
     const int nh = blockIdx.x;
+    const int c0 = blockIdx.y * DEC_CW;
     const int tid = threadIdx.x;
     const int d = p.d, dv = p.dv;
+    const int width = min(DEC_CW, dv - c0);
+    const int ncg = width >> 2;
+    const int R = DEC_NT / ncg;
+    const int cg = tid % ncg, rg = tid / ncg;
+    const int nrows = rg < R ? (d - rg + R - 1) / R : 0;  // rows rg, rg+R, ... < d (threads past R*ncg idle)
+    const int rs4 = dv >> 2;                               // row stride of M in float4
+    float4* M4 = reinterpret_cast<float4*>(p.M + (int64_t)nh * d * dv + c0) + cg;
+    float4 m[MAXR];
+#pragma unroll
+    for (int r = 0; r < MAXR; ++r)
+        if (r < nrows) m[r] = __ldcs(M4 + (int64_t)(rg + r * R) * rs4);
+
     const TI* q = static_cast<const TI*>(p.q) + (int64_t)nh * d;
     const TI* k = static_cast<const TI*>(p.k) + (int64_t)nh * d;
-    const TI* v = static_cast<const TI*>(p.v) + (int64_t)nh * dv;
+    const TI* v = static_cast<const TI*>(p.v) + (int64_t)nh * dv + c0;
+    float zo = 0.f;
     if (tid < d) {
+        zo = p.z[(int64_t)nh * d + tid];
         fq[tid] = phi_f(ldf(q + tid));
         fk[tid] = phi_f(ldf(k + tid));
     }
-    if (tid < dv) vv[tid] = ldf(v + tid);
+    if (tid < width) vv[tid] = ldf(v + tid);
     __syncthreads();
-    // z <- z + phi(k); den = phi(q) . z + eps
+    // z <- z + phi(k) (written by the first column block); den = phi(q) . z + eps
     float part = 0.f;
     if (tid < d) {
-        float* zp = p.z + (int64_t)nh * d + tid;
-        const float zn = *zp + fk[tid];
-        *zp = zn;
+        const float zn = zo + fk[tid];
+        if (blockIdx.y == 0) p.z[(int64_t)nh * d + tid] = zn;
         part = fq[tid] * zn;
     }
     for (int off = 16; off; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
     if ((tid & 31) == 0) dred[tid >> 5] = part;
 
-    const int ncg = dv >> 2;
-    const int R = 256 / ncg;
-    const int cg = tid % ncg, rg = tid / ncg;
-    const int nrows = rg < R ? (d - rg + R - 1) / R : 0;  // rows rg, rg+R, ... < d (threads past R*ncg idle)
-    float4* M4 = reinterpret_cast<float4*>(p.M + (int64_t)nh * d * dv) + cg;
     const float4 v4 = reinterpret_cast<const float4*>(vv)[cg];
-    float4 m[MAXR];
-#pragma unroll
-    for (int r = 0; r < MAXR; ++r)
-        if (r < nrows) m[r] = __ldcs(M4 + (int64_t)(rg + r * R) * ncg);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < MAXR; ++r) {
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeParams p) {
             x.y = fmaf(a, v4.y, x.y);
             x.z = fmaf(a, v4.z, x.z);
             x.w = fmaf(a, v4.w, x.w);
-            __stcs(M4 + (int64_t)i * ncg, x);
+            __stcs(M4 + (int64_t)i * rs4, x);
             acc.x = fmaf(g, x.x, acc.x);
             acc.y = fmaf(g, x.y, acc.y);
             acc.z = fmaf(g, x.z, acc.z);
@@ -337,8 +349,9 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeParams p) {
             s.z += x.z;
             s.w += x.w;
         }
-        const float den = dred[0] + dred[1] + dred[2] + dred[3] + dred[4] + dred[5] + dred[6] + dred[7] + p.eps;
-        TI* o = static_cast<TI*>(p.out) + (int64_t)nh * dv + tid * 4;
+        float den = p.eps;
+        for (int w = 0; w < 4; ++w) den += dred[w];  // threads >= d (<= 128) add nothing
+        TI* o = static_cast<TI*>(p.out) + (int64_t)nh * dv + c0 + tid * 4;
         stf(o + 0, s.x / den);
         stf(o + 1, s.y / den);
         stf(o + 2, s.z / den);
@@ -400,9 +413,9 @@ cudaError_t launch_prefill_out(const PrefillOutParams& p, bool bf16, cudaStream_
 
 cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s) {
     if (bf16)
-        decode_kernel<__nv_bfloat16><<<p.N * p.H, 256, 0, s>>>(p);
+        decode_kernel<__nv_bfloat16><<<dim3(p.N * p.H, (p.dv + DEC_CW - 1) / DEC_CW), DEC_NT, 0, s>>>(p);
     else
-        decode_kernel<float><<<p.N * p.H, 256, 0, s>>>(p);
+        decode_kernel<float><<<dim3(p.N * p.H, (p.dv + DEC_CW - 1) / DEC_CW), DEC_NT, 0, s>>>(p);
     return cudaGetLastError();
 }
 

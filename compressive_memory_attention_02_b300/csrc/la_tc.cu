@@ -7,10 +7,11 @@
 //             and its sum can be formed in parallel pieces). Used for prefill parts
 //             and for the range aggregates of the sequence-split forward.
 //
-// Roles in a block of 192 threads: warp 0 lane 0 issues TMA loads into a 4-stage
+// Roles in a block of 320 threads: warp 0 lane 0 issues TMA loads into a 4-stage
 // ring, warp 1 owns TMEM and lane 0 issues tcgen05.mma (M^T (dv x d) += V_c^T phi(K_c),
-// f32 accumulator in TMEM), warps 2-5 apply phi in place and keep column sums of
-// phi(K) for s_p. TMEM lane quarter q = warp % 4 is accessible to that warp only.
+// f32 accumulator in TMEM), warps 2-9 (two per sub-partition) apply phi in place and
+// keep column sums of phi(K) for s_p, then write the record. TMEM lane quarter
+// q = warp % 4 is accessible to that warp only.
 //
 // Operand layouts (128-byte swizzled, 1024-byte aligned atoms of 8 rows x 128 bytes,
 // 16-byte chunk c of row r stored at chunk c ^ (r % 8)): K and V tiles exactly as TMA
@@ -21,6 +22,9 @@
 namespace la {
 
 // ============================================================================ parts_tc
+constexpr int PARTS_FW = 8;  // phi warps
+constexpr int PARTS_THREADS = 64 + 32 * PARTS_FW;
+
 template <int D, int DV>
 struct PartsLayout {
     static constexpr int NS = 4;
@@ -32,12 +36,12 @@ struct PartsLayout {
     static constexpr int NBAR = 3 * NS + 1;
     static constexpr int MISC = BAR + 8 * NBAR;          // tmem holder, abort flag
     static constexpr int ZP = MISC + 16;
-    static constexpr int TOTAL = ZP + 4 * D * 4;
+    static constexpr int TOTAL = ZP + PARTS_FW * D * 4;
     static constexpr int ALLOC = TOTAL + 1024;           // slack for 1024-byte alignment
 };
 
 template <int D, int DV>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(PARTS_THREADS, 1)
     parts_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, PartsParams p) {
     using L = PartsLayout<D, DV>;
     constexpr int NS = L::NS;
@@ -125,7 +129,8 @@ __global__ void __launch_bounds__(192, 1)
             mma_commit(done);
             mbar_wait_drain(done, 0);
         }
-    } else {  // ------------------------ compute warps
+    } else {  // ------------------------ phi warps
+        constexpr int NT = 32 * PARTS_FW;
         const int ct = threadIdx.x - 64;
         float colsum[8];
 #pragma unroll
@@ -133,33 +138,37 @@ __global__ void __launch_bounds__(192, 1)
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
             const int s = c % NS;
-            ok = bar_and(1, 128, mbar_wait(&full[s], (c / NS) & 1, abort_flag));
+            ok = bar_and(1, NT, mbar_wait(&full[s], (c / NS) & 1, abort_flag));
             if (!ok) break;
             const int valid = (int)min64(CH, t_end - (t_begin + (int64_t)c * CH));
-            phi_tile<D>(sm + s * L::STAGE, ATOM, valid, ct, colsum);
+            phi_tile<D, NT>(sm + s * L::STAGE, ATOM, valid, ct, colsum);
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
+            named_bar_sync(1, NT);
             if (ct == 0) mbar_arrive(&phib[s]);
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
-        ok = bar_and(1, 128, ok && mbar_wait(done, 0, abort_flag));
+        ok = bar_and(1, NT, ok && mbar_wait(done, 0, abort_flag));
         colsum_to_smem<D>(colsum, zpart, ct);
-        named_bar_sync(1, 128);
+        named_bar_sync(1, NT);
         if (ok) {
             tc_fence_after();
             const int64_t rec = (int64_t)bh * p.nparts + part;
             if (ct < D) {
-                float zz = zpart[ct] + zpart[D + ct] + zpart[2 * D + ct] + zpart[3 * D + ct];
+                float zz = 0.f;
+#pragma unroll
+                for (int w = 0; w < PARTS_FW; ++w) zz += zpart[w * D + ct];
                 if (p.base_z) zz += p.base_z[(int64_t)bh * D + ct];
                 p.dst_z[rec * p.rec_z + ct] = zz;
             }
+            // warps 2-5 write columns [0, 64) of the record's rows, warps 6-9 columns [64, 128)
             const int q = warp & 3;
-            if (32 * q < DV) {  // warp-uniform
+            const int c_lo = (warp - 2) / 4 * 64;
+            if (32 * q < DV && c_lo < D) {  // warp-uniform
                 const int j = 32 * q + lane;
                 float* dst = p.dst_M + rec * p.rec_M + j;
                 const float* base = p.base_M ? p.base_M + (int64_t)bh * D * DV + j : nullptr;
 #pragma unroll 1
-                for (int i0 = 0; i0 < D; i0 += 32) {
+                for (int i0 = c_lo; i0 < c_lo + 64; i0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + i0, r);
                     tmem_wait_ld();
@@ -192,7 +201,7 @@ static cudaError_t launch_parts_tc_t(const PartsParams& p, const CUtensorMap& mk
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     dim3 grid(p.nparts, p.B * p.H);
-    fn<<<grid, 192, L::ALLOC, s>>>(mk, mv, p);
+    fn<<<grid, PARTS_THREADS, L::ALLOC, s>>>(mk, mv, p);
     return cudaGetLastError();
 }
 

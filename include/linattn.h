@@ -177,6 +177,14 @@ int la_get_last_device_status(la_stream_t stream);
 
 const char* la_get_error_string(int code);
 
+/* Failure-path self-test: launches one block that waits on a barrier nothing ever
+ * completes, with a limit of `limit_cycles` SM clock cycles (1 .. 2^32); the wait runs
+ * out, the kernel records LA_ERR_TIMEOUT in this device's status word and returns, so
+ * the next la_get_last_device_status reports LA_ERR_TIMEOUT and the context stays usable.
+ * It checks the same bounded-wait and status path that every kernel's mbarrier waits use.
+ * Returns LA_ERR_INVALID_ARG for a limit outside that range. */
+int la_selftest_wait_timeout(unsigned long long limit_cycles, la_stream_t stream);
+
 /* Number of kernels the most recent call on this host thread launched. */
 int la_last_launch_count(void);
 
