@@ -40,6 +40,7 @@ __device__ __forceinline__ void record_timeout(int* status, volatile int* abort_
 
 // Bounded wait that ignores the abort flag (used while draining at exit).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (clock64() - t0 > LA_WAIT_CYCLES) return false;
