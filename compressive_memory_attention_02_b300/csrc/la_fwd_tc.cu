@@ -12,16 +12,17 @@
 // operand (read from tensor memory) of the next chunk's inter-chunk MMA; the state
 // never passes through shared memory.
 //
-// One block per (range, head). Warp roles (768 threads; warp w issues on sub-partition
+// One block per (range, head). Warp roles (1024 threads; warp w issues on sub-partition
 // w % 4 and may touch only TMEM lane quarter w % 4):
 //   warp 0        TMA producer: Q, K, V tiles into a 3-stage ring
 //   warp 1        TMEM owner; lane 0 issues every tcgen05.mma, software-pipelined one
 //                 chunk ahead: PV_c, then S'_{c+1}, inter_{c+1}, update_{c+1}
-//   warps 2,3,18-23  F: phi in place on Q and K, zero padded keys, column sums -> z
+//   warps 2,3,18-31  F: phi in place on Q and K, zero padded keys, column sums -> z
 //   warps 4-7     R: bf16 re-cast of M^T after each update; final M to global memory
-//   warps 8-15    E: initial state into TMEM; then out = O / den -> bf16, 8 x 8
-//                 transposes across lanes (O^T holds one feature per lane) -> swizzled
-//                 smem tile -> TMA store; warps 8-11 take tokens 0-31, 12-15 tokens 32-63
+//   warps 8-15    E: initial state into TMEM; then out = O / den -> bf16 -> swizzled
+//                 smem tile (O^T holds one feature per lane: fragments loaded in the
+//                 accumulator layout are stored transposed with stmatrix) -> TMA store;
+//                 warps 8-11 take tokens 0-31, 12-15 tokens 32-63
 //   warps 16,17   S: P and 1/den from S'
 // Each hand-off is an mbarrier; TMEM reads and writes are ordered with tcgen05 fences
 // around it.
@@ -40,8 +41,8 @@
 
 namespace la {
 
-constexpr int FWD_THREADS = 768;
-constexpr int NFW = 8;  // F warps
+constexpr int FWD_THREADS = 1024;
+constexpr int NFW = 16;  // F warps
 
 template <int D, int DV>
 struct FwdLayout {
@@ -70,10 +71,10 @@ constexpr uint32_t TM_A = 128;   // M^T bf16, two per column: d/2 columns (A ope
 __device__ __forceinline__ uint32_t tm_s(int buf) { return 192u + 80u * buf; }  // S', 80 columns each
 __device__ __forceinline__ uint32_t tm_o(int buf) { return 352u + 64u * buf; }  // O^T, 64 columns each
 
-// 32 f32 values -> 16 words of two bf16 (low half = even index)
-__device__ __forceinline__ void pack32_bf16(const uint32_t* x, uint32_t* a) {
+// 16 f32 values -> 8 words of two bf16 (low half = even index)
+__device__ __forceinline__ void pack16_bf16(const uint32_t* x, uint32_t* a) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) a[k] = pack_bf16(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1]));
+    for (int k = 0; k < 8; ++k) a[k] = pack_bf16(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1]));
 }
 
 template <int D, int DV>
@@ -258,12 +259,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         auto recast = [&]() {
             if (!has_row) return;
 #pragma unroll 1
-            for (int i0 = 0; i0 < D; i0 += 32) {
-                uint32_t x[32], a[16];
-                tmem_ld32(tmem + TM_M + lane_base + i0, x);
+            for (int i0 = 0; i0 < D; i0 += 16) {
+                uint32_t x[16], a[8];
+                tmem_ld16(tmem + TM_M + lane_base + i0, x);
                 tmem_wait_ld();
-                pack32_bf16(x, a);
-                tmem_st16(tmem + TM_A + lane_base + i0 / 2, a);
+                pack16_bf16(x, a);
+                tmem_st8(tmem + TM_A + lane_base + i0 / 2, a);
             }
             tmem_wait_st();
         };
@@ -282,12 +283,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             } else if (writes_state && p.M_out && has_row) {
                 float* dst = p.M_out + (int64_t)bh * D * DV + j;
 #pragma unroll 1
-                for (int i0 = 0; i0 < D; i0 += 32) {
-                    uint32_t x[32];
-                    tmem_ld32(tmem + TM_M + lane_base + i0, x);
+                for (int i0 = 0; i0 < D; i0 += 16) {
+                    uint32_t x[16];
+                    tmem_ld16(tmem + TM_M + lane_base + i0, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) dst[(int64_t)(i0 + e) * DV] = __uint_as_float(x[e]);
+                    for (int e = 0; e < 16; ++e) dst[(int64_t)(i0 + e) * DV] = __uint_as_float(x[e]);
                 }
             }
         }
@@ -304,25 +305,24 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             // column j of the initial state M_in (+ range aggregates), rows [64hf, 64hf + 64)
             const float* src = p.M_in ? p.M_in + (int64_t)bh * D * DV + j : nullptr;
 #pragma unroll 1
-            for (int i0 = 64 * hf; i0 < D && i0 < 64 * hf + 64; i0 += 32) {
-                uint32_t x[32], a[16];
+            for (int i0 = 64 * hf; i0 < D && i0 < 64 * hf + 64; i0 += 16) {
+                uint32_t x[16], a[8];
                 if (src) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__ldg(src + (int64_t)(i0 + e) * DV));
+                    for (int e = 0; e < 16; ++e) x[e] = __float_as_uint(__ldg(src + (int64_t)(i0 + e) * DV));
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = 0u;
+                    for (int e = 0; e < 16; ++e) x[e] = 0u;
                 }
 #pragma unroll 1
                 for (int pp = 0; pp < nws; ++pp) {
                     const float* ag = agg + pp * p.rec + (int64_t)i0 * DV + j;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) + __ldg(ag + e * DV));
+                    for (int e = 0; e < 16; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) + __ldg(ag + e * DV));
                 }
                 tmem_st16(tmem + TM_M + lane_base + i0, x);
-                tmem_st16(tmem + TM_M + lane_base + i0 + 16, x + 16);
-                pack32_bf16(x, a);
-                tmem_st16(tmem + TM_A + lane_base + i0 / 2, a);
+                pack16_bf16(x, a);
+                tmem_st8(tmem + TM_A + lane_base + i0 / 2, a);
             }
             tmem_wait_st();
         }
@@ -330,12 +330,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         named_bar_sync(3, 256);
         if (ct == 0) mbar_arrive(mt_ready);
 
-        // Lane l holds feature j of the chunk's outputs. After an 8 x 8 transpose within its
-        // group of 8 lanes it holds token t (t % 8 == l % 8) of the features j0 .. j0+7,
-        // j0 = 32q + 8(l / 8): one 16-byte chunk of the [token][feature] tile.
-        const int i8 = lane & 7;
-        const int j0 = 32 * q + (lane & ~7);
-        uint8_t* obase = sm + L::OT + (j0 >> 6) * ATOM + ((((j0 & 63) >> 3) ^ i8) << 4);
+        // Thread l of the warp stores, per stmatrix, row (l % 8) of matrix l / 8: features
+        // f0 .. f0+7 (f0 = 32q + 8(l / 8)) of token 32hf + 8i + (l % 8), i = 0..3; the row's
+        // 16-byte chunk of the swizzled [token][feature] tile:
+        const int f0 = 32 * q + 8 * (lane >> 3);
+        const uint32_t ot_row = smem_u32(sm + L::OT + (f0 >> 6) * ATOM) + (uint32_t)((((f0 & 63) >> 3) ^ (lane & 7)) << 4);
         const uint64_t pol = l2_evict_first_policy();  // out is written once
         bool ok = true;
         for (int m = 0; m < n_main; ++m) {
@@ -347,18 +346,24 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (ct == 0) tma_store_wait_read0();  // previous out tile read by the TMA unit
             named_bar_sync(3, 256);
             if (has_row) {
-                const float4* rd4 = reinterpret_cast<const float4*>(rden + buf * 64);
-#pragma unroll 1
-                for (int bb = 4 * hf; bb < 4 * hf + 4; ++bb) {  // tokens 8bb .. 8bb+7 (compact: see phi_tile)
-                    uint32_t x[8];
-                    tmem_ld8(tmem + tm_o(buf) + lane_base + 8 * bb, x);
-                    const float4 ra = rd4[2 * bb], rb = rd4[2 * bb + 1];
-                    tmem_wait_ld();
-                    const float* xs = reinterpret_cast<const float*>(x);
-                    uint32_t w[4] = {pack_bf16(xs[0] * ra.x, xs[1] * ra.y), pack_bf16(xs[2] * ra.z, xs[3] * ra.w),
-                                     pack_bf16(xs[4] * rb.x, xs[5] * rb.y), pack_bf16(xs[6] * rb.z, xs[7] * rb.w)};
-                    transpose8x8_b16(w, lane);
-                    *reinterpret_cast<uint4*>(obase + (8 * bb + i8) * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+                // O^T lanes 32q + 16lb + {0..15}, tokens 32hf + {0..31}: two loads in the fragment layout
+                uint32_t x[2][16];
+                tmem_ld16x256_x4(tmem + tm_o(buf) + lane_base + 32 * hf, x[0]);
+                tmem_ld16x256_x4(tmem + tm_o(buf) + lane_base + (16u << 16) + 32 * hf, x[1]);
+                const float2* rd2 = reinterpret_cast<const float2*>(rden + buf * 64 + 32 * hf + 2 * (lane & 3));
+                float2 rd[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) rd[i] = rd2[4 * i];  // tokens 8i + 2(l % 4) + {0, 1}
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t w[4];  // matrix m = 2lb + hh: features 32q + 16lb + 8hh + {0..7}, tokens 8i + {0..7}
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t* r = x[m >> 1] + 4 * i + 2 * (m & 1);
+                        w[m] = pack_bf16(__uint_as_float(r[0]) * rd[i].x, __uint_as_float(r[1]) * rd[i].y);
+                    }
+                    stmatrix_x4_trans(ot_row + (uint32_t)((32 * hf + 8 * i + (lane & 7)) * 128), w);
                 }
             }
             tc_fence_before();
@@ -392,22 +397,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             uint8_t* prow = sm + L::PT + buf * ATOM + t * 128;
             float rowsum = 0.f;
 #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                uint32_t x[32];
-                tmem_ld32(tmem + tm_s(buf) + lane_base + 32 * half, x);
+            for (int qt = 0; qt < 4; ++qt) {  // keys 16qt .. 16qt+15
+                uint32_t x[16];
+                tmem_ld16(tmem + tm_s(buf) + lane_base + 16 * qt, x);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                uint32_t pk[8];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int c0 = 32 * half + 2 * jj;
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int c0 = 16 * qt + 2 * jj;
                     const float s0 = (c0 <= t) ? __uint_as_float(x[2 * jj]) : 0.f;
                     const float s1 = (c0 + 1 <= t) ? __uint_as_float(x[2 * jj + 1]) : 0.f;
                     pk[jj] = pack_bf16(s0, s1);
                     rowsum += bf16lo(pk[jj]) + bf16hi(pk[jj]);
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c2 = 4 * half + u;
+                for (int u = 0; u < 2; ++u) {
+                    const int c2 = 2 * qt + u;
                     *reinterpret_cast<uint4*>(prow + ((c2 ^ (t & 7)) << 4)) =
                         make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 }
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
     } else {
-        // ======================================================== F: phi and z (warps 2, 3, 18-23)
+        // ======================================================== F: phi and z (warps 2, 3, 18-31)
         const int ct = (warp < 4 ? warp - 2 : warp - 16) * 32 + lane;
         if (ct < D) {
             float zz = p.z_in ? p.z_in[(int64_t)bh * D + ct] : 0.f;

@@ -63,33 +63,6 @@ __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Transpose an 8 x 8 matrix of 16-bit values held by 8 consecutive lanes (lane i of the
-// group holds row i as four words of two values, low half first) so that lane i ends
-// up with column i. Three exchange steps over lane distances 4, 2, 1 swap blocks of
-// 4 x 4, 2 x 2 and single elements.
-__device__ __forceinline__ void transpose8x8_b16(uint32_t (&r)[4], int lane) {
-    const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
-    uint32_t s0 = b2 ? r[0] : r[2], s1 = b2 ? r[1] : r[3];
-    s0 = __shfl_xor_sync(0xffffffffu, s0, 4);
-    s1 = __shfl_xor_sync(0xffffffffu, s1, 4);
-    if (b2) r[0] = s0, r[1] = s1;
-    else r[2] = s0, r[3] = s1;
-    s0 = b1 ? r[0] : r[1];
-    s1 = b1 ? r[2] : r[3];
-    s0 = __shfl_xor_sync(0xffffffffu, s0, 2);
-    s1 = __shfl_xor_sync(0xffffffffu, s1, 2);
-    if (b1) r[0] = s0, r[2] = s1;
-    else r[1] = s0, r[3] = s1;
-    const uint32_t sel_send = b0 ? 0x5410u : 0x7632u;  // even lanes send their high halves, odd the low
-    s0 = __shfl_xor_sync(0xffffffffu, __byte_perm(r[0], r[1], sel_send), 1);
-    s1 = __shfl_xor_sync(0xffffffffu, __byte_perm(r[2], r[3], sel_send), 1);
-    const uint32_t sa = b0 ? 0x3254u : 0x5410u, sb = b0 ? 0x3276u : 0x7610u;
-    r[0] = __byte_perm(r[0], s0, sa);
-    r[1] = __byte_perm(r[1], s0, sb);
-    r[2] = __byte_perm(r[2], s1, sa);
-    r[3] = __byte_perm(r[3], s1, sb);
-}
-
 // phi in place on a [64 x D] bf16 tile (atoms `astride` bytes apart), by NT threads.
 // Thread ct owns 16-byte chunk column j = ct % (D/8) of rows g, g + RG, ...
 // (g = ct / (D/8)); since RG is a multiple of 8 the swizzled chunk position
