@@ -83,9 +83,13 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, 
     for (int i = 0; i < RPT; ++i) {
         uint4 x = base[i * RG * 8];
         uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        const bool live = g + i * RG < valid;
+        if (g + i * RG < valid) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) w[e] = live ? phi_bf16x2(w[e]) : 0u;
+            for (int e = 0; e < 4; ++e) w[e] = phi_bf16x2(w[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = 0u;
+        }
         base[i * RG * 8] = make_uint4(w[0], w[1], w[2], w[3]);
         if (colsum) {
 #pragma unroll
