@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             uint8_t* prow = sm + L::PT + buf * ATOM + t * 128;
-            float rowsum = 0.f;
+            uint64_t rowsum2 = 0;  // (even keys, odd keys) partial sums
 #pragma unroll 1
             for (int qt = 0; qt < 4; ++qt) {  // keys 16qt .. 16qt+15
                 uint32_t x[16];
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                     const float s0 = (c0 <= t) ? __uint_as_float(x[2 * jj]) : 0.f;
                     const float s1 = (c0 + 1 <= t) ? __uint_as_float(x[2 * jj + 1]) : 0.f;
                     pk[jj] = pack_bf16(s0, s1);
-                    rowsum += bf16lo(pk[jj]) + bf16hi(pk[jj]);
+                    rowsum2 = f2_add(rowsum2, f2_pack(bf16lo(pk[jj]), bf16hi(pk[jj])));
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             uint32_t zc[16];
             tmem_ld16(tmem + tm_s(buf) + lane_base + 64, zc);
             tmem_wait_ld();
-            rden[buf * 64 + t] = 1.f / (__uint_as_float(zc[0]) + rowsum + p.eps);
+            rden[buf * 64 + t] = 1.f / (__uint_as_float(zc[0]) + (f2_lo(rowsum2) + f2_hi(rowsum2)) + p.eps);
             tc_fence_before();
             fence_proxy_async_smem();
             named_bar_sync(2, 64);

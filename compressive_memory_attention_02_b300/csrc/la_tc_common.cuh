@@ -58,7 +58,8 @@ __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
     const __nv_bfloat162 mn = __hmin2(x, zero);
     const uint32_t m = *reinterpret_cast<const uint32_t*>(&mn);
     constexpr float kLog2e = 1.4426950408889634f;
-    const __nv_bfloat162 e = __floats2bfloat162_rn(ex2_approx(bf16lo(m) * kLog2e), ex2_approx(bf16hi(m) * kLog2e));
+    const uint64_t y = f2_mul(f2_pack(bf16lo(m), bf16hi(m)), f2_pack(kLog2e, kLog2e));
+    const __nv_bfloat162 e = __floats2bfloat162_rn(ex2_approx(f2_lo(y)), ex2_approx(f2_hi(y)));
     const __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
     return *reinterpret_cast<const uint32_t*>(&r);
 }
@@ -79,6 +80,11 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, 
     constexpr int RPT = CH / RG;
     const int j = ct % CPR, g = ct / CPR;
     uint4* base = reinterpret_cast<uint4*>(tile + (j >> 3) * astride + (((j & 7) ^ (g & 7)) << 4) + g * 128);
+    uint64_t cs[4];  // column sums as f32 pairs
+    if (colsum) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cs[e] = f2_pack(colsum[2 * e], colsum[2 * e + 1]);
+    }
 #pragma unroll 1
     for (int i = 0; i < RPT; ++i) {
         uint4 x = base[i * RG * 8];
@@ -93,11 +99,12 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, 
         base[i * RG * 8] = make_uint4(w[0], w[1], w[2], w[3]);
         if (colsum) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                colsum[2 * e] += bf16lo(w[e]);
-                colsum[2 * e + 1] += bf16hi(w[e]);
-            }
+            for (int e = 0; e < 4; ++e) cs[e] = f2_add(cs[e], f2_pack(bf16lo(w[e]), bf16hi(w[e])));
         }
+    }
+    if (colsum) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) colsum[2 * e] = f2_lo(cs[e]), colsum[2 * e + 1] = f2_hi(cs[e]);
     }
 }
 
