@@ -358,10 +358,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     uint32_t w[4];  // matrix m = 2lb + hh: features 32q + 16lb + 8hh + {0..7}, tokens 8i + {0..7}
+                    const uint64_t rdi = f2_pack(rd[i].x, rd[i].y);
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         const uint32_t* r = x[m >> 1] + 4 * i + 2 * (m & 1);
-                        w[m] = pack_bf16(__uint_as_float(r[0]) * rd[i].x, __uint_as_float(r[1]) * rd[i].y);
+                        const uint64_t o = f2_mul(f2_pack(__uint_as_float(r[0]), __uint_as_float(r[1])), rdi);
+                        w[m] = pack_bf16(f2_lo(o), f2_hi(o));
                     }
                     stmatrix_x4_trans(ot_row + (uint32_t)((32 * hf + 8 * i + (lane & 7)) * 128), w);
                 }
