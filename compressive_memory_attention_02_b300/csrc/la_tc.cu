@@ -7,8 +7,8 @@
 //             and its sum can be formed in parallel pieces). Used for prefill parts
 //             and for the range aggregates of the sequence-split forward.
 //
-// Roles in a block of 320 threads: warp 0 lane 0 issues TMA loads into a 4-stage
-// ring, warp 1 owns TMEM and lane 0 issues tcgen05.mma (M^T (dv x d) += V_c^T phi(K_c),
+// Roles in a block of 320 threads (two blocks per SM): warp 0 lane 0 issues TMA loads
+// into a 3-stage ring, warp 1 owns TMEM and lane 0 issues tcgen05.mma (M^T (dv x d) += V_c^T phi(K_c),
 // f32 accumulator in TMEM), warps 2-9 (two per sub-partition) apply phi in place and
 // keep column sums of phi(K) for s_p, then write the record. TMEM lane quarter
 // q = warp % 4 is accessible to that warp only.
@@ -27,7 +27,7 @@ constexpr int PARTS_THREADS = 64 + 32 * PARTS_FW;
 
 template <int D, int DV>
 struct PartsLayout {
-    static constexpr int NS = 4;
+    static constexpr int NS = 3;   // 3 stages keep two blocks on an SM (~109 KB each)
     static constexpr int KB = D / 64 * ATOM;
     static constexpr int VB = DV / 64 * ATOM;
     static constexpr int STAGE = KB + VB;
@@ -41,7 +41,7 @@ struct PartsLayout {
 };
 
 template <int D, int DV>
-__global__ void __launch_bounds__(PARTS_THREADS, 1)
+__global__ void __launch_bounds__(PARTS_THREADS, 2)
     parts_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, PartsParams p) {
     using L = PartsLayout<D, DV>;
     constexpr int NS = L::NS;
