@@ -65,15 +65,17 @@ def algorithmic(w):
     return bytes_qkvo + state, th * flops_per_th
 
 
+FWD_SOURCES = ("la_fwd_tc.cu", "la_internal.h", "la_ptx.cuh", "la_tc_common.cuh")
+
+
 def kernel_source_sha():
-    """sha256 over the library's CUDA sources (csrc/*.cu, *.cuh, *.h, sorted by name)."""
+    """sha256 over the sources the forward kernel is compiled from."""
     import hashlib
     d = os.path.join(ROOT, "compressive_memory_attention_02_b300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in FWD_SOURCES:
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
