@@ -171,7 +171,7 @@ static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dt
         P = 2;
     }
     if (ws_avail < alias_bytes) return pl;
-    const int pct = env_int("LA_FWD_SPLIT_PCT", 70);
+    const int pct = env_int("LA_FWD_SPLIT_PCT", 66);
     int64_t split = (nch * pct + 50) / 100;
     split = std::max<int64_t>(1, std::min<int64_t>(split, nch - 1));
     pl.nranges = 2;

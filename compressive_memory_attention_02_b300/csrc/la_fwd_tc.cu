@@ -446,6 +446,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         }
         named_bar_sync(1, 32 * NFW);
         bool ok = true;
+        float colsum_agg[8];  // state-only chunks: column sums kept in registers, folded once at the end
+#pragma unroll
+        for (int e = 0; e < 8; ++e) colsum_agg[e] = 0.f;
         for (int g = 0; g < nchunks; ++g) {
             const int s = g % NST;
             const bool is_main = g >= n_agg;
@@ -458,16 +461,26 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (is_main && ct < D)  // row 64 (a multiple of 8: no swizzle offset) carries z before this chunk
                 *reinterpret_cast<__nv_bfloat16*>(kb + (ct >> 6) * ATOMK + 64 * 128 + (ct & 63) * 2) =
                     __float2bfloat16_rn(zf[ct]);
+            if (!is_main) {
+                // z is needed only after the last state-only chunk: no per-chunk reduction
+                phi_tile<D, 32 * NFW>(kb, ATOMK, valid, ct, colsum_agg);
+                fence_proxy_async_smem();
+                named_bar_sync(1, 32 * NFW);
+                if (ct == 0) mbar_arrive(&phib[s]);
+                if (g + 1 < n_agg) continue;
+            }
             float colsum[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) colsum[e] = 0.f;
-            if (is_main) phi_tile<D, 32 * NFW>(qb, ATOM, CH, ct, nullptr);
-            phi_tile<D, 32 * NFW>(kb, ATOMK, valid, ct, colsum);
+            for (int e = 0; e < 8; ++e) colsum[e] = is_main ? 0.f : colsum_agg[e];
+            if (is_main) {
+                phi_tile<D, 32 * NFW>(qb, ATOM, CH, ct, nullptr);
+                phi_tile<D, 32 * NFW>(kb, ATOMK, valid, ct, colsum);
+            }
             float* zp = zpart + (g & 1) * NFW * D;
             colsum_to_smem<D>(colsum, zp, ct);
-            fence_proxy_async_smem();
+            if (is_main) fence_proxy_async_smem();
             named_bar_sync(1, 32 * NFW);
-            if (ct == 0) mbar_arrive(&phib[s]);
+            if (ct == 0 && is_main) mbar_arrive(&phib[s]);
             if (ct < D) {
                 float zz = zf[ct];
 #pragma unroll
