@@ -139,6 +139,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
+    // above may overlap that kernel's tail, but nothing in global memory is read or written
+    // before it has completed. This block lets the next such launch start its own set-up.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
 
     if (warp == 0) {
         // ======================================================== TMA producer
@@ -508,9 +513,17 @@ static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, 
     auto fn = fwd_tc_kernel<D, DV>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.nranges, B * p.H);
-    fn<<<grid, FWD_THREADS, L::ALLOC, s>>>(mq, mk, mv, mo, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nranges, B * p.H);
+    cfg.blockDim = dim3(FWD_THREADS);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, mq, mk, mv, mo, p);
 }
 
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
