@@ -106,7 +106,7 @@ def peaks():
 
 class _Nvml:
     """Minimal ctypes binding of the NVML calls the sampler needs (libnvidia-ml ships
-    with the driver; the pynvml wrapper may not be installed)."""
+    with the NVIDIA display driver; the pynvml wrapper may not be installed)."""
     SM = 1  # NVML_CLOCK_SM
 
     def __init__(self, cuda_index):
