@@ -455,8 +455,9 @@ def _graph_time(call, reps, dev):
 
 
 def run_modes(dev):
-    """The other two modes on their workloads: prefill (B=1 H=8 T=1,048,576, final state and
-    last output) and decode steps (256 streams x 32 heads). Kernel-only device time."""
+    """The other workloads: prefill (B=1 H=8 T=1,048,576, final state and last output), the
+    training-style forward (B=4 H=16 T=4096 d=dv=64, one call) and decode steps (256 streams
+    x 32 heads). Kernel-only device time."""
     import torch
 
     import compressive_memory_attention_02_b300 as la
@@ -489,6 +490,25 @@ def run_modes(dev):
                                    "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                    "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs"}}
     del q, k, v, ws
+
+    w = synthetic.WORKLOADS["train"]
+    B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
+    q, k, v = (bf(a) for a in synthetic.qkv(w))
+    out = torch.empty(B, H, T, dv, dtype=torch.bfloat16, device=dev)
+    M = torch.empty(B, H, d, dv, device=dev)
+    z = torch.empty(B, H, d, device=dev)
+    nws = la.la_causal_fwd_workspace_size(B, H, T, d, dv, w.chunk, la.LA_BF16)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+    ms = _graph_time(lambda: la.la_causal_fwd_ex(q, k, v, out, None, None, M, z, B, H, T, d, dv, w.chunk, w.eps,
+                                                 la.LA_BF16, None, ws, nws), 20, dev)
+    assert la.la_get_last_device_status() == la.LA_OK
+    byt = B * H * T * (2 * d + 2 * dv) * 2 + B * H * (d * dv + d) * 4
+    res["train_fwd"] = {"workload": f"B={B} H={H} T={T} d=dv={d} bf16, chunk {w.chunk}, all outputs + final M,z",
+                        "value": round(B * T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(ms, 5),
+                        "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
+                                     "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                                     "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs"}}
+    del q, k, v, out, ws
 
     w = synthetic.WORKLOADS["generation"]
     N, H, d, dv = w.B, w.H, w.d, w.dv
