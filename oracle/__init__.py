@@ -8,6 +8,11 @@ Contents
   causal_fwd / prefill / decode_step   the token recurrence in plain C (la_oracle.c),
                                        page "Attention_Kernel_Mask", section
                                        "Implementing Causality with Cumulative Sums"
+  causal_bwd                           its training backward: the chain rule on that
+                                       recurrence, a forward sweep for dq and a reverse
+                                       sweep carrying the state gradient (la_oracle.c);
+                                       the page's mode table names the training-backward
+                                       mode but prints no formula
   brute_force                          the same outputs from the lower-triangular
                                        (masked O(T^2)) form of that page's question
                                        about multiplying by an all-ones lower-
@@ -65,8 +70,11 @@ def _load():
         lib.oracle_decode_step.argtypes = [vp, vp, vp, c_int, vp, vp, vp,
                                            i64, i64, c_int, c_int, dbl, c_int]
         lib.oracle_phi.argtypes = [vp, vp, i64]
+        lib.oracle_causal_bwd.argtypes = [vp, vp, vp, c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          i64, i64, i64, c_int, c_int, dbl, c_int]
         lib.oracle_max_threads.restype = c_int
-        for f in (lib.oracle_causal_fwd, lib.oracle_prefill, lib.oracle_decode_step, lib.oracle_phi):
+        for f in (lib.oracle_causal_fwd, lib.oracle_prefill, lib.oracle_decode_step, lib.oracle_phi,
+                  lib.oracle_causal_bwd):
             f.restype = None
         _lib = lib
     return _lib
@@ -149,6 +157,34 @@ def decode_step(q, k, v, M, z, eps=1e-6, mutation=0):
                                M2.ctypes.data, z2.ctypes.data, out.ctypes.data,
                                N, H, d, dv, float(eps), int(mutation))
     return out, M2, z2
+
+
+def causal_bwd(q, k, v, dout, M_in=None, z_in=None, dM_out=None, dz_out=None, eps=1e-6, mutation=0):
+    """Training backward: the gradients of L = sum(dout * out) + sum(dM_out * M_T) +
+    sum(dz_out * z_T) with respect to the float64 values of q, k, v (storage arrays,
+    as for causal_fwd) and of the initial state. dout [B,H,T,dv], dM_out [B,H,d,dv],
+    dz_out [B,H,d] are float64 (the state gradients may be None = zero).
+    Returns (dq, dk, dv, dM_in, dz_in), all float64."""
+    q, k, v = _c(q), _c(k), _c(v)
+    assert q.dtype == k.dtype == v.dtype
+    B, H, T, d = q.shape
+    dv = v.shape[3]
+    M_in = _state_or_none(M_in, (B, H, d, dv))
+    z_in = _state_or_none(z_in, (B, H, d))
+    dM_out = _state_or_none(dM_out, (B, H, d, dv))
+    dz_out = _state_or_none(dz_out, (B, H, d))
+    dout = np.ascontiguousarray(dout, dtype=np.float64)
+    assert dout.shape == (B, H, T, dv)
+    dq = np.empty((B, H, T, d))
+    dk = np.empty((B, H, T, d))
+    dvv = np.empty((B, H, T, dv))
+    dM_in = np.empty((B, H, d, dv))
+    dz_in = np.empty((B, H, d))
+    _load().oracle_causal_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, _dtype_code(q),
+                              _ptr(M_in), _ptr(z_in), dout.ctypes.data, _ptr(dM_out), _ptr(dz_out),
+                              dq.ctypes.data, dk.ctypes.data, dvv.ctypes.data, dM_in.ctypes.data,
+                              dz_in.ctypes.data, B, H, T, d, dv, float(eps), int(mutation))
+    return dq, dk, dvv, dM_in, dz_in
 
 
 def phi(x) -> np.ndarray:

@@ -190,6 +190,162 @@ void oracle_decode_step(const void* q, const void* k, const void* v, int dtype,
     }
 }
 
+/* ------------------------------------------------------------------------
+ * Training backward (float64).
+ *
+ * Gradients of a scalar loss L whose gradients with respect to the forward's
+ * outputs are given: dout_t for every output, dM_out and dz_out for the final
+ * state. The pages name a training-backward mode (page "Attention_Kernel_Mask",
+ * table "Causal Attention Training and Inferencing") but print no formula, so
+ * this is the chain rule applied to the recurrence above, token by token:
+ *   forward sweep, t = 0 .. T-1 (z_t and M_t include token t):
+ *       g_t = dout_t / D_t               gradient of phi(q_t)^T M_t
+ *       e_t = -(g_t . out_t)             gradient of D_t
+ *       dphi(q_t) = M_t g_t + e_t z_t
+ *   reverse sweep, i = T-1 .. 0, from R = dM_out and r = dz_out:
+ *       R += phi(q_i) g_i^T,  r += e_i phi(q_i)   (every read at t >= i sees token i)
+ *       dphi(k_i) = R v_i + r,  dv_i = R^T phi(k_i)
+ *   after the sweep dM_in = R and dz_in = r; dx = dphi(x) phi'(x), where
+ *   phi'(x) = 1 for x > 0 and exp(x) otherwise.
+ *
+ * mutation (pin tests only): 11 drop e_t z_t from dphi(q_t); 12 use the state
+ * before token t in dphi(q_t); 13 ignore dM_out and dz_out; 14 use R and r before
+ * adding token i's own term; 15 phi' = 1 everywhere; 16 dv_i = R phi(k_i) read
+ * over the other index (d == dv only).
+ */
+static inline double dphi(double x, int mutation) {
+    if (mutation == 15) return 1.0;
+    return x > 0.0 ? 1.0 : exp(x);
+}
+
+static void stream_bwd(const void* q, const void* k, const void* v, int dtype, int64_t qoff, int64_t voff,
+                       int64_t T, int d, int dv, double eps, double* M, double* z, const double* dout,
+                       const double* dM_out, const double* dz_out, double* dq, double* dk, double* dvv,
+                       double* dM_in, double* dz_in, int mutation) {
+    double* fq_all = (double*)malloc(sizeof(double) * (size_t)(T * d));
+    double* g_all = (double*)malloc(sizeof(double) * (size_t)(T * dv));
+    double* e_all = (double*)malloc(sizeof(double) * (size_t)T);
+    double* fk = (double*)malloc(sizeof(double) * (size_t)d);
+    double* vv = (double*)malloc(sizeof(double) * (size_t)dv);
+    double* o = (double*)malloc(sizeof(double) * (size_t)dv);
+    double* R = (double*)malloc(sizeof(double) * (size_t)d * dv);
+    double* r = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int64_t t = 0; t < T; ++t) {
+        double* fq = fq_all + t * d;
+        double* g = g_all + t * dv;
+        for (int i = 0; i < d; ++i) {
+            fq[i] = phi(widen(q, dtype, qoff + t * d + i), 0);
+            fk[i] = phi(widen(k, dtype, qoff + t * d + i), 0);
+        }
+        for (int j = 0; j < dv; ++j) vv[j] = widen(v, dtype, voff + t * dv + j);
+        for (int i = 0; i < d; ++i) {
+            z[i] += fk[i];
+            double* row = M + (int64_t)i * dv;
+            for (int j = 0; j < dv; ++j) row[j] += fk[i] * vv[j];
+        }
+        double den = eps;
+        for (int i = 0; i < d; ++i) den += fq[i] * z[i];
+        for (int j = 0; j < dv; ++j) o[j] = 0.0;
+        for (int i = 0; i < d; ++i) {
+            const double* row = M + (int64_t)i * dv;
+            for (int j = 0; j < dv; ++j) o[j] += fq[i] * row[j];
+        }
+        double e = 0.0;
+        for (int j = 0; j < dv; ++j) {
+            o[j] /= den;
+            g[j] = dout[t * dv + j] / den;
+            e -= g[j] * o[j];
+        }
+        e_all[t] = e;
+        for (int i = 0; i < d; ++i) {
+            const double* row = M + (int64_t)i * dv;
+            double s = 0.0;
+            for (int j = 0; j < dv; ++j) s += row[j] * g[j];
+            double zi = z[i];
+            if (mutation == 12) {   /* planted: state before token t */
+                double vg = 0.0;
+                for (int j = 0; j < dv; ++j) vg += vv[j] * g[j];
+                s -= fk[i] * vg;
+                zi -= fk[i];
+            }
+            if (mutation != 11) s += e * zi;
+            dq[t * d + i] = s * dphi(widen(q, dtype, qoff + t * d + i), mutation);
+        }
+    }
+    for (int64_t a = 0; a < (int64_t)d * dv; ++a) R[a] = (dM_out && mutation != 13) ? dM_out[a] : 0.0;
+    for (int i = 0; i < d; ++i) r[i] = (dz_out && mutation != 13) ? dz_out[i] : 0.0;
+    for (int64_t t = T - 1; t >= 0; --t) {
+        const double* fq = fq_all + t * d;
+        const double* g = g_all + t * dv;
+        for (int i = 0; i < d; ++i) fk[i] = phi(widen(k, dtype, qoff + t * d + i), 0);
+        for (int j = 0; j < dv; ++j) vv[j] = widen(v, dtype, voff + t * dv + j);
+        if (mutation != 14) {
+            for (int i = 0; i < d; ++i) {
+                double* row = R + (int64_t)i * dv;
+                for (int j = 0; j < dv; ++j) row[j] += fq[i] * g[j];
+                r[i] += e_all[t] * fq[i];
+            }
+        }
+        for (int i = 0; i < d; ++i) {
+            const double* row = R + (int64_t)i * dv;
+            double s = r[i];
+            for (int j = 0; j < dv; ++j) s += row[j] * vv[j];
+            dk[t * d + i] = s * dphi(widen(k, dtype, qoff + t * d + i), mutation);
+        }
+        for (int j = 0; j < dv; ++j) {
+            double s = 0.0;
+            if (mutation == 16) {
+                for (int i = 0; i < d && i < dv; ++i) s += R[(int64_t)j * dv + i] * fk[i];
+            } else {
+                for (int i = 0; i < d; ++i) s += R[(int64_t)i * dv + j] * fk[i];
+            }
+            dvv[t * dv + j] = s;
+        }
+        if (mutation == 14) {
+            for (int i = 0; i < d; ++i) {
+                double* row = R + (int64_t)i * dv;
+                for (int j = 0; j < dv; ++j) row[j] += fq[i] * g[j];
+                r[i] += e_all[t] * fq[i];
+            }
+        }
+    }
+    if (dM_in) memcpy(dM_in, R, sizeof(double) * (size_t)d * dv);
+    if (dz_in) memcpy(dz_in, r, sizeof(double) * (size_t)d);
+    free(fq_all);
+    free(g_all);
+    free(e_all);
+    free(fk);
+    free(vv);
+    free(o);
+    free(R);
+    free(r);
+}
+
+/* q, k: [B, H, T, d], v: [B, H, T, dv] storage arrays (dtype as above); dout
+ * [B, H, T, dv], dM_out [B, H, d, dv], dz_out [B, H, d] float64 (the two state
+ * gradients may be NULL = zero); M_in, z_in float64 (NULL = zero state).
+ * Outputs float64: dq, dk [B, H, T, d], dv [B, H, T, dv], dM_in, dz_in (may be NULL). */
+void oracle_causal_bwd(const void* q, const void* k, const void* v, int dtype,
+                       const double* M_in, const double* z_in, const double* dout,
+                       const double* dM_out, const double* dz_out,
+                       double* dq, double* dk, double* dvv, double* dM_in, double* dz_in,
+                       int64_t B, int64_t H, int64_t T, int d, int dv, double eps, int mutation) {
+    const int64_t BH = B * H;
+    const int64_t ms = (int64_t)d * dv;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double* M = (double*)malloc(sizeof(double) * (size_t)ms);
+        double* z = (double*)malloc(sizeof(double) * (size_t)d);
+        load_state(M_in, z_in, bh, d, dv, M, z);
+        stream_bwd(q, k, v, dtype, bh * T * d, bh * T * dv, T, d, dv, eps, M, z, dout + bh * T * dv,
+                   dM_out ? dM_out + bh * ms : NULL, dz_out ? dz_out + bh * d : NULL,
+                   dq + bh * T * d, dk + bh * T * d, dvv + bh * T * dv,
+                   dM_in ? dM_in + bh * ms : NULL, dz_in ? dz_in + bh * d : NULL, mutation);
+        free(M);
+        free(z);
+    }
+}
+
 /* phi on its own, for the pin tests. */
 void oracle_phi(const double* x, double* y, int64_t n) {
     for (int64_t i = 0; i < n; ++i) y[i] = phi(x[i], 0);
