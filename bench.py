@@ -456,8 +456,8 @@ def _graph_time(call, reps, dev):
 
 def run_modes(dev):
     """The other workloads: prefill (B=1 H=8 T=1,048,576, final state and last output), the
-    training-style forward (B=4 H=16 T=4096 d=dv=64, one call) and decode steps (256 streams
-    x 32 heads). Kernel-only device time."""
+    training-style forward and backward (B=4 H=16 T=4096 d=dv=64, one call each) and decode
+    steps (256 streams x 32 heads). Kernel-only device time."""
     import torch
 
     import compressive_memory_attention_02_b300 as la
@@ -508,7 +508,28 @@ def run_modes(dev):
                         "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
                                      "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                      "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs"}}
-    del q, k, v, out, ws
+
+    # training backward on the same inputs: dout seeded, zero initial state, dM_in and dz_in written
+    dout = bf(synthetic.normal(w.seed, 7, (B, H, T, dv), 1.0, "bf16"))
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dM = torch.empty(B, H, d, dv, device=dev)
+    dz = torch.empty(B, H, d, device=dev)
+    nws = la.la_causal_bwd_workspace_size(B, H, T, d, dv)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    ms = _graph_time(lambda: la.la_causal_bwd_ex(q, k, v, dout, None, None, None, None, dq, dk, dvv, dM, dz, B, H, T,
+                                                 d, dv, w.eps, la.LA_BF16, ws, nws), 5, dev)
+    assert la.la_get_last_device_status() == la.LA_OK
+    byt = B * H * T * (4 * d + 3 * dv) * 2 + B * H * (d * dv + d) * 4
+    C, nch = 64, (T + 63) // 64
+    flops = 2 * B * H * nch * (5 * C * d * dv + C * (C + 1) // 2 * (3 * d + 4 * dv))
+    res["train_bwd"] = {"workload": f"B={B} H={H} T={T} d=dv={d} bf16, dout ~ N(0,1), dq, dk, dv + dM_in, dz_in",
+                        "value": round(B * T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(ms, 5),
+                        "launches": 6,
+                        "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
+                                     "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                                     "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs",
+                                     "fp32_simt_tflops": round(flops / (ms / 1e3) / 1e12, 2)}}
+    del q, k, v, out, ws, dout, dq, dk, dvv
 
     w = synthetic.WORKLOADS["generation"]
     N, H, d, dv = w.B, w.H, w.d, w.dv

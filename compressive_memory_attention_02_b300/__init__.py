@@ -23,7 +23,8 @@ LA_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's static prefill scra
 EXPORTS = (
     "la_causal_fwd", "la_causal_fwd_ex", "la_causal_fwd_workspace_size",
     "la_prefill_state", "la_prefill_state_ex", "la_prefill_workspace_size", "la_prefill_state_noalloc",
-    "la_decode_step", "la_set_workspace", "la_get_last_device_status",
+    "la_decode_step", "la_causal_bwd", "la_causal_bwd_ex", "la_causal_bwd_workspace_size",
+    "la_set_workspace", "la_get_last_device_status",
     "la_get_error_string", "la_last_launch_count", "la_selftest_wait_timeout",
 )
 
@@ -52,6 +53,11 @@ def _load() -> ctypes.CDLL:
     lib.la_prefill_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32]
     lib.la_prefill_workspace_size.restype = sz
     lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
+    bwd = [vp] * 13 + [i32, i32, i64, i32, i32, f32, i32]
+    lib.la_causal_bwd.argtypes = bwd + [vp]
+    lib.la_causal_bwd_ex.argtypes = bwd + [vp, sz, vp]
+    lib.la_causal_bwd_workspace_size.argtypes = [i32, i32, i64, i32, i32]
+    lib.la_causal_bwd_workspace_size.restype = sz
     lib.la_set_workspace.argtypes = [vp, sz]
     lib.la_get_last_device_status.argtypes = [vp]
     lib.la_get_error_string.argtypes = [i32]
@@ -64,6 +70,7 @@ def _load() -> ctypes.CDLL:
             f.restype = i32
     lib.la_causal_fwd_workspace_size.restype = sz
     lib.la_prefill_workspace_size.restype = sz
+    lib.la_causal_bwd_workspace_size.restype = sz
     lib.la_get_error_string.restype = ctypes.c_char_p
     return lib
 
@@ -166,6 +173,27 @@ def la_decode_step(q, k, v, out, M, z, N, H, d, dv, eps, dtype=None, stream=None
     rc = lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(M), _ptr(z), N, H, d, dv, eps,
                             _dtype(dtype, q), _stream(stream, q))
     return _check("la_decode_step", rc)
+
+
+def la_causal_bwd(q, k, v, dout, M_in, z_in, dM_out, dz_out, dq, dk, dv, dM_in, dz_in, B, H, T, d, dv_dim, eps,
+                  dtype=None, stream=None):
+    rc = lib.la_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(M_in), _ptr(z_in), _ptr(dM_out),
+                           _ptr(dz_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dM_in), _ptr(dz_in), B, H, T, d, dv_dim,
+                           eps, _dtype(dtype, q), _stream(stream, q))
+    return _check("la_causal_bwd", rc)
+
+
+def la_causal_bwd_ex(q, k, v, dout, M_in, z_in, dM_out, dz_out, dq, dk, dv, dM_in, dz_in, B, H, T, d, dv_dim, eps,
+                     dtype=None, workspace=None, workspace_bytes=0, stream=None):
+    rc = lib.la_causal_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(M_in), _ptr(z_in), _ptr(dM_out),
+                              _ptr(dz_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dM_in), _ptr(dz_in), B, H, T, d,
+                              dv_dim, eps, _dtype(dtype, q), _ptr(workspace), int(workspace_bytes),
+                              _stream(stream, q))
+    return _check("la_causal_bwd_ex", rc)
+
+
+def la_causal_bwd_workspace_size(B, H, T, d, dv) -> int:
+    return int(lib.la_causal_bwd_workspace_size(B, H, T, d, dv))
 
 
 def la_set_workspace(ptr, nbytes):

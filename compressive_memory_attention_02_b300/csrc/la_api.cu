@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/linattn.h"
+#include "la_bwd.h"
 #include "la_internal.h"
 
 namespace la {
@@ -400,6 +401,73 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
     return LA_OK;
 }
 
+// Training backward behind la_causal_bwd / la_causal_bwd_ex: six launches on `stream`
+// (la_bwd.cu), scratch from the registered workspace (use_registered) or (ws, ws_bytes).
+static int bwd_impl(const void* q, const void* k, const void* v, const void* dout, const float* M_in,
+                    const float* z_in, const float* dM_out, const float* dz_out, void* dq, void* dk, void* dv,
+                    float* dM_in, float* dz_in, int B, int H, int64_t T, int d, int dv_dim, float eps,
+                    la_dtype dtype, void* ws, size_t ws_bytes, bool use_registered, cudaStream_t stream) {
+    t_launches = 0;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return LA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || T <= 0 || !(eps >= 0.f)) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+    if (!shape_ok(d, dv_dim)) return LA_ERR_UNSUPPORTED;
+    const int64_t BH = (int64_t)B * H;
+    const int64_t nch = ceil_div(T, BWD_CH);
+    if (BH > 65535 || nch > 0x7fffffff) return LA_ERR_UNSUPPORTED;
+    const void* ins[4] = {q, k, v, dout};
+    void* outs[3] = {dq, dk, dv};
+    for (void* o : outs)
+        for (const void* i : ins)
+            if (o == i) return LA_ERR_INVALID_ARG;
+    if (dq == dk || dq == dv || dk == dv) return LA_ERR_INVALID_ARG;
+    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return LA_ERR_WORKSPACE;
+    DeviceState* ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc) return rc;
+    if (use_registered) ws = ds->ws, ws_bytes = ds->ws_bytes;
+    size_t off_rev = 0, off_G = 0, off_E = 0;
+    const size_t need = sizeof(float) * bwd_workspace_floats(BH, T, d, dv_dim, &off_rev, &off_G, &off_E);
+    if (!ws || ws_bytes < need) return LA_ERR_WORKSPACE;
+    float* wsf = static_cast<float*>(ws);
+    const int64_t rec = (int64_t)d * dv_dim + d;
+    const bool bf16 = dtype == LA_BF16;
+
+    PartsParams pp{};  // 64-token key-value sums
+    pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv_dim;
+    pp.rec_M = rec, pp.rec_z = rec;
+    pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv_dim;
+    pp.part_len = BWD_CH, pp.nparts = (int)nch, pp.eps = eps, pp.st = contiguous(H, T, d, dv_dim);
+    pp.status = ds->status;
+    if ((rc = cuda_rc(launch_parts_simt(pp, bf16, stream)))) return rc;
+    ++t_launches;
+
+    ScanParams sp{};  // states before each chunk
+    sp.rec = wsf, sp.base_M = M_in, sp.base_z = z_in, sp.BH = (int)BH, sp.nch = (int)nch;
+    sp.d = d, sp.dv = dv_dim, sp.len = rec, sp.reverse = false;
+    if ((rc = cuda_rc(launch_scan_states(sp, stream)))) return rc;
+    ++t_launches;
+
+    BwdParams bp{};
+    bp.q = q, bp.k = k, bp.v = v, bp.dout = dout, bp.dq = dq, bp.dk = dk, bp.dv = dv;
+    bp.states = wsf, bp.rev = wsf + off_rev, bp.G = wsf + off_G, bp.E = wsf + off_E;
+    bp.B = B, bp.H = H, bp.T = T, bp.d = d, bp.dv_dim = dv_dim, bp.nch = (int)nch, bp.rec = rec, bp.eps = eps;
+    if ((rc = cuda_rc(launch_bwd_dq(bp, bf16, stream)))) return rc;
+    ++t_launches;
+
+    ScanParams rp{};  // state gradient from every token after each chunk; totals = dM_in, dz_in
+    rp.rec = wsf + off_rev, rp.base_M = dM_out, rp.base_z = dz_out, rp.total_M = dM_in, rp.total_z = dz_in;
+    rp.BH = (int)BH, rp.nch = (int)nch, rp.d = d, rp.dv = dv_dim, rp.len = rec, rp.reverse = true;
+    if ((rc = cuda_rc(launch_scan_states(rp, stream)))) return rc;
+    ++t_launches;
+
+    if ((rc = cuda_rc(launch_bwd_dk(bp, bf16, stream)))) return rc;
+    ++t_launches;
+    if ((rc = cuda_rc(launch_bwd_dv(bp, bf16, stream)))) return rc;
+    ++t_launches;
+    return LA_OK;
+}
+
 }  // namespace la
 
 using namespace la;
@@ -470,6 +538,27 @@ int la_decode_step(const void* q, const void* k, const void* v, void* out, float
     return rc;
 }
 
+int la_causal_bwd(const void* q, const void* k, const void* v, const void* dout, const float* M_in, const float* z_in,
+                  const float* dM_out, const float* dz_out, void* dq, void* dk, void* dv, float* dM_in, float* dz_in,
+                  int B, int H, int64_t T, int d, int dv_dim, float eps, la_dtype dtype, la_stream_t stream) {
+    return bwd_impl(q, k, v, dout, M_in, z_in, dM_out, dz_out, dq, dk, dv, dM_in, dz_in, B, H, T, d, dv_dim, eps,
+                    dtype, nullptr, 0, true, (cudaStream_t)stream);
+}
+
+int la_causal_bwd_ex(const void* q, const void* k, const void* v, const void* dout, const float* M_in,
+                     const float* z_in, const float* dM_out, const float* dz_out, void* dq, void* dk, void* dv,
+                     float* dM_in, float* dz_in, int B, int H, int64_t T, int d, int dv_dim, float eps, la_dtype dtype,
+                     void* workspace, size_t workspace_bytes, la_stream_t stream) {
+    return bwd_impl(q, k, v, dout, M_in, z_in, dM_out, dz_out, dq, dk, dv, dM_in, dz_in, B, H, T, d, dv_dim, eps,
+                    dtype, workspace, workspace_bytes, false, (cudaStream_t)stream);
+}
+
+size_t la_causal_bwd_workspace_size(int B, int H, int64_t T, int d, int dv) {
+    if (B <= 0 || H <= 0 || T <= 0 || !shape_ok(d, dv)) return 0;
+    size_t a = 0, b = 0, c = 0;
+    return sizeof(float) * bwd_workspace_floats((int64_t)B * H, T, d, dv, &a, &b, &c);
+}
+
 int la_set_workspace(void* ptr, size_t bytes) {
     if (ptr && (reinterpret_cast<uintptr_t>(ptr) & 255u)) return LA_ERR_WORKSPACE;
     DeviceState* ds = nullptr;
@@ -502,7 +591,7 @@ const char* la_get_error_string(int code) {
         case LA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
         case LA_ERR_CUDA: return "CUDA runtime or launch failure";
         case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
-        case LA_ERR_WORKSPACE: return "workspace pointer not 256-byte aligned";
+        case LA_ERR_WORKSPACE: return "workspace pointer not 256-byte aligned, or too small for a call that needs one";
         case LA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's static buffer holds";
         default: return "unknown error";
     }

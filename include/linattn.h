@@ -60,7 +60,7 @@ enum {
     LA_ERR_UNSUPPORTED = 2,   /* d, dv, chunk or dtype outside the supported set */
     LA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
     LA_ERR_TIMEOUT = 4,       /* device status: a bounded wait inside a kernel ran out */
-    LA_ERR_WORKSPACE = 5,     /* workspace pointer misaligned */
+    LA_ERR_WORKSPACE = 5,     /* workspace pointer misaligned, or too small for la_causal_bwd */
     LA_ERR_SCRATCH_LIMIT = 6  /* la_prefill_state_noalloc: the problem needs more scratch than
                                  LA_NOALLOC_SCRATCH_BYTES */
 };
@@ -163,6 +163,43 @@ int la_prefill_state_noalloc(const void* q, const void* k, const void* v, void* 
 int la_decode_step(const void* q, const void* k, const void* v, void* out,
                    float* M, float* z, int N, int H, int d, int dv, float eps,
                    la_dtype dtype, la_stream_t stream);
+
+/* ---- training backward -----------------------------------------------------------
+ * Gradients of the training forward (the mode table's training-backward row; the page
+ * prints no formula, so these are the chain rule on the chunk form above). For a scalar
+ * loss L with given dL/dout (dout), dL/dM_out and dL/dz_out, with D_t the denominator
+ * and g_t = dout_t / D_t, e_t = -(g_t . out_t):
+ *   dq_t = (M_t g_t + e_t z_t) o phi'(q_t)
+ *   dk_i = (R_i v_i + r_i) o phi'(k_i),   dv_i = R_i^T phi(k_i)
+ *   R_i = dM_out + sum_{t >= i} phi(q_t) g_t^T,   r_i = dz_out + sum_{t >= i} e_t phi(q_t)
+ *   dM_in = R_0,   dz_in = r_0
+ * (M_t, z_t include token t; phi'(x) = 1 for x > 0, exp(x) otherwise; "o" is the
+ * elementwise product). The forward quantities are recomputed from q, k, v, M_in, z_in
+ * in float32; nothing from the forward call is needed.
+ *   q, k [B,H,T,d], v, dout [B,H,T,dv]  dtype, contiguous, read
+ *   M_in, z_in        float32, read (NULL = zero initial state)
+ *   dM_out, dz_out    float32 [B,H,d,dv] / [B,H,d], read (NULL = zero)
+ *   dq, dk [B,H,T,d], dv [B,H,T,dv]  dtype, contiguous, written; must not alias an input
+ *                     or each other
+ *   dM_in, dz_in      float32, written (NULL = not wanted); may equal dM_out / dz_out
+ * Scratch: la_causal_bwd_workspace_size(B, H, T, d, dv) bytes (two float32 state records
+ * per 64-token chunk and head, plus T*(dv+1) floats per head), from the registered
+ * workspace (la_causal_bwd) or `workspace` (la_causal_bwd_ex, 256-byte aligned); with
+ * less, the call returns LA_ERR_WORKSPACE and launches nothing. Six kernel launches on
+ * `stream`. Supported: the forward's d, dv and dtypes; B*H <= 65535. */
+int la_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                  const float* M_in, const float* z_in, const float* dM_out, const float* dz_out,
+                  void* dq, void* dk, void* dv, float* dM_in, float* dz_in,
+                  int B, int H, int64_t T, int d, int dv_dim, float eps, la_dtype dtype,
+                  la_stream_t stream);
+
+int la_causal_bwd_ex(const void* q, const void* k, const void* v, const void* dout,
+                     const float* M_in, const float* z_in, const float* dM_out, const float* dz_out,
+                     void* dq, void* dk, void* dv, float* dM_in, float* dz_in,
+                     int B, int H, int64_t T, int d, int dv_dim, float eps, la_dtype dtype,
+                     void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+size_t la_causal_bwd_workspace_size(int B, int H, int64_t T, int d, int dv);
 
 /* ---- runtime -------------------------------------------------------------------
  * la_set_workspace: register (ptr, bytes) as the scratch of the plain calls on

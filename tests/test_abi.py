@@ -71,3 +71,25 @@ def test_decode_and_prefill_reject_bad_arguments_on_host():
     assert la.lib.la_prefill_state(16, 32, 48, 64, None, None, None, None, 1, 1, 64, 64, 64, -1, 1e-6, 1,
                                    None) == la.LA_ERR_INVALID_ARG
     assert la.lib.la_set_workspace(8, 1024) == la.LA_ERR_WORKSPACE
+
+
+def test_backward_workspace_size_and_host_checks():
+    """Size of the backward's scratch: two float32 state records per 64-token chunk and
+    head, plus T*(dv+1) floats per head, each region rounded up to 256 bytes; argument
+    errors are found on the host before anything is launched."""
+    import compressive_memory_attention_02_b300 as la
+    up = lambda n: (n + 63) // 64 * 64
+    for B, H, T, d, dv in [(1, 1, 1, 8, 8), (2, 3, 130, 64, 32), (4, 16, 4096, 64, 64), (2, 32, 2048, 128, 128)]:
+        BH, nch, rec = B * H, (T + 63) // 64, d * dv + d
+        want = 4 * (2 * up(BH * nch * rec) + up(BH * T * dv) + up(BH * T))
+        assert la.la_causal_bwd_workspace_size(B, H, T, d, dv) == want
+    assert la.la_causal_bwd_workspace_size(1, 1, 64, 12, 64) == 0   # d not a multiple of 8
+    assert la.la_causal_bwd_workspace_size(1, 1, 0, 64, 64) == 0
+    args = [16, 32, 48, 64, None, None, None, None, 80, 96, 112, None, None]
+    assert la.lib.la_causal_bwd(*args, 1, 1, 64, 64, 64, 1e-6, 1, None) in (la.LA_ERR_WORKSPACE, la.LA_ERR_CUDA)
+    assert la.lib.la_causal_bwd(*args, 1, 1, 64, 60, 64, 1e-6, 1, None) == la.LA_ERR_UNSUPPORTED
+    assert la.lib.la_causal_bwd(*args, 1, 1, 0, 64, 64, 1e-6, 1, None) == la.LA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[8] = 16  # dq aliases q
+    assert la.lib.la_causal_bwd(*bad, 1, 1, 64, 64, 64, 1e-6, 1, None) == la.LA_ERR_INVALID_ARG
+    assert la.lib.la_causal_bwd(*args, 1, 1, 64, 64, 64, 1e-6, 3, None) == la.LA_ERR_UNSUPPORTED
