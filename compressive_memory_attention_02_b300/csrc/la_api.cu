@@ -421,6 +421,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
         for (const void* i : ins)
             if (o == i) return LA_ERR_INVALID_ARG;
     if (dq == dk || dq == dv || dk == dv) return LA_ERR_INVALID_ARG;
+    for (const void* a : ins)  // read as 16-byte vectors
+        if (!aligned16(a)) return LA_ERR_INVALID_ARG;
     if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return LA_ERR_WORKSPACE;
     DeviceState* ds = nullptr;
     int rc = current_device(&ds);
@@ -433,13 +435,11 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
     const int64_t rec = (int64_t)d * dv_dim + d;
     const bool bf16 = dtype == LA_BF16;
 
-    PartsParams pp{};  // 64-token key-value sums
-    pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv_dim;
-    pp.rec_M = rec, pp.rec_z = rec;
-    pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv_dim;
-    pp.part_len = BWD_CH, pp.nparts = (int)nch, pp.eps = eps, pp.st = contiguous(H, T, d, dv_dim);
-    pp.status = ds->status;
-    if ((rc = cuda_rc(launch_parts_simt(pp, bf16, stream)))) return rc;
+    BwdParams bp{};
+    bp.q = q, bp.k = k, bp.v = v, bp.dout = dout, bp.dq = dq, bp.dk = dk, bp.dv = dv;
+    bp.states = wsf, bp.rev = wsf + off_rev, bp.G = wsf + off_G, bp.E = wsf + off_E;
+    bp.B = B, bp.H = H, bp.T = T, bp.d = d, bp.dv_dim = dv_dim, bp.nch = (int)nch, bp.rec = rec, bp.eps = eps;
+    if ((rc = cuda_rc(launch_bwd_sums(bp, bf16, stream)))) return rc;  // 64-token key-value sums
     ++t_launches;
 
     ScanParams sp{};  // states before each chunk
@@ -448,10 +448,6 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
     if ((rc = cuda_rc(launch_scan_states(sp, stream)))) return rc;
     ++t_launches;
 
-    BwdParams bp{};
-    bp.q = q, bp.k = k, bp.v = v, bp.dout = dout, bp.dq = dq, bp.dk = dk, bp.dv = dv;
-    bp.states = wsf, bp.rev = wsf + off_rev, bp.G = wsf + off_G, bp.E = wsf + off_E;
-    bp.B = B, bp.H = H, bp.T = T, bp.d = d, bp.dv_dim = dv_dim, bp.nch = (int)nch, bp.rec = rec, bp.eps = eps;
     if ((rc = cuda_rc(launch_bwd_dq(bp, bf16, stream)))) return rc;
     ++t_launches;
 

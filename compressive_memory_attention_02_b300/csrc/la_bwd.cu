@@ -15,12 +15,13 @@
 //   dM_in = dM_out + sum over all chunks of phi(Q_c)^T G_c   (dz_in the same with e)
 // and dx = dphi(x) phi'(x), where phi'(x) = min(phi(x), 1): 1 for x > 0, exp(x) otherwise.
 //
-// Launches (la_api.cu): 64-token key-value sums (parts_simt) -> exclusive prefix scan
+// Launches (la_api.cu): 64-token key-value sums (bwd_sums) -> exclusive prefix scan
 // (the state before each chunk) -> bwd_dq (dq, G, E and the chunk sums phi(Q)^T G,
 // phi(Q)^T e) -> exclusive reverse scan (R_c; the totals are dM_in, dz_in) -> bwd_dk ->
 // bwd_dv. A chunk kernel runs one block of 256 threads per (chunk, b*H + h) with every
-// operand of the chunk in shared memory; tile rows are padded by one float so that
-// column-wise reads by consecutive threads fall in distinct banks.
+// operand of the chunk in shared memory (tile rows padded by one float so that strided
+// reads by consecutive threads fall in distinct banks); its products run through Tile,
+// a register-tiled micro-kernel.
 #include "la_bwd.h"
 
 namespace la {
@@ -57,62 +58,163 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Rows 0..C-1 of a contiguous [rows, n] slice into a tile with row stride ld (phi applied
-// when asked); rows >= nv become 0.
+// 16 bytes of storage elements -> floats (8 for bf16, 4 for float32).
+__device__ __forceinline__ void unpack16(const uint4& u, float* x, const __nv_bfloat16*) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void unpack16(const uint4& u, float* x, const float*) {
+    x[0] = __uint_as_float(u.x), x[1] = __uint_as_float(u.y), x[2] = __uint_as_float(u.z), x[3] = __uint_as_float(u.w);
+}
+
+// Rows 0..C-1 of a contiguous [rows, n] slice (16-byte aligned, n a multiple of 8) into a
+// tile with row stride ld, phi applied when asked; rows >= nv become 0. Every thread
+// issues all of its 16-byte loads (at most 8) before it uses any of them.
 template <typename TI>
 __device__ void load_rows(float* dst, int ld, const TI* src, int n, int nv, bool apply_phi) {
-    for (int idx = threadIdx.x; idx < C * n; idx += NT) {
-        const int t = idx / n, i = idx - t * n;
-        float x = 0.f;
-        if (t < nv) {
-            x = bld(src + (int64_t)t * n + i);
-            if (apply_phi) x = phi_f(x);
-        }
-        dst[t * ld + i] = x;
+    constexpr int VE = 16 / (int)sizeof(TI);
+    const int vpr = n / VE, nvec = C * vpr;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4 buf[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = (int)threadIdx.x + u * NT;
+        buf[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < nvec && idx / vpr < nv) buf[u] = __ldg(s4 + idx);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = (int)threadIdx.x + u * NT;
+        if (idx >= nvec) break;
+        const int t = idx / vpr, c0 = (idx - t * vpr) * VE;
+        float x[8];
+        unpack16(buf[u], x, src);
+        const bool f = apply_phi && t < nv;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) dst[t * ld + c0 + e] = f ? phi_f(x[e]) : x[e];
     }
 }
 
-// A state record (M row-major d x dv, then z) into Ms (row stride ld) and zs.
+// A state record (M row-major d x dv, then z; 16-byte aligned) into Ms (row stride ld) and zs.
 __device__ void load_record(float* Ms, int ld, float* zs, const float* rec, int d, int dv) {
-    for (int idx = threadIdx.x; idx < d * dv; idx += NT) {
-        const int i = idx / dv, j = idx - i * dv;
-        Ms[i * ld + j] = rec[idx];
+    const int nvec = d * dv / 4, vpr = dv / 4;
+    const float4* s4 = reinterpret_cast<const float4*>(rec);
+    for (int base = 0; base < nvec; base += 8 * NT) {
+        float4 buf[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + (int)threadIdx.x + u * NT;
+            if (idx < nvec) buf[u] = __ldg(s4 + idx);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + (int)threadIdx.x + u * NT;
+            if (idx >= nvec) break;
+            const int i = idx / vpr, j = (idx - i * vpr) * 4;
+            float* m = Ms + i * ld + j;
+            m[0] = buf[u].x, m[1] = buf[u].y, m[2] = buf[u].z, m[3] = buf[u].w;
+        }
     }
     for (int i = threadIdx.x; i < d; i += NT) zs[i] = rec[(int64_t)d * dv + i];
 }
 
-// S_tj = phi(q_t) . phi(k_j) for j <= t, else 0.
-__device__ void scores(float* Ss, const float* Qf, const float* Kf, int ldq, int d) {
-    for (int o = threadIdx.x; o < C * C; o += NT) {
-        const int t = o / C, j = o - t * C;
-        float acc = 0.f;
-        if (j <= t) {
-            const float* a = Qf + t * ldq;
-            const float* b = Kf + j * ldq;
-            for (int i = 0; i < d; ++i) acc = fmaf(a[i], b[i], acc);
-        }
-        Ss[t * LDS + j] = acc;
+// Register-tiled product over shared-memory operands: out(r, n) += sum_k A(r, k) B(k, n)
+// with A(r, k) = A[r*ars + k*aks] and B(k, n) = B[k*bks + n*bns]. Thread (rg, cg) =
+// (tid / 16, tid % 16) owns rows r0 + rg + 16i (i < 4) and columns cg + 16j (j < 8, while
+// below N): per k it loads 4 + (up to) 8 operands for up to 32 multiply-adds. Rows past
+// R read row R-1 (in bounds) and are not stored.
+struct Tile {
+    float acc[4][8];
+    int rg, cg, nb;
+    __device__ explicit Tile(int N) : rg((int)threadIdx.x >> 4), cg((int)threadIdx.x & 15) {
+        nb = (N - cg + 15) >> 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
     }
+    __device__ void add(const float* A, int ars, int aks, const float* B, int bks, int bns, int K, int r0, int R) {
+        int ro[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ro[i] = min(r0 + rg + 16 * i, R - 1) * ars;
+        for (int k = 0; k < K; ++k) {
+            float a[4], b[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = A[ro[i] + k * aks];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) b[j] = (j < nb) ? B[k * bks + (cg + 16 * j) * bns] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < nb) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+    }
+    // f(row, col, value) for every owned element with row < R
+    template <class F>
+    __device__ void store(int r0, int R, F f) const {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = r0 + rg + 16 * i;
+            if (r >= R) continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < nb) f(r, cg + 16 * j, acc[i][j]);
+        }
+    }
+};
+
+// S_tj = phi(q_t) . phi(k_j) for j <= t, else 0 (the C x C product, then the mask).
+__device__ void scores(float* Ss, const float* Qf, const float* Kf, int ldq, int d) {
+    Tile tl(C);
+    tl.add(Qf, ldq, 1, Kf, 1, ldq, d, 0, C);
+    tl.store(0, C, [&](int t, int j, float x) { Ss[t * LDS + j] = (j <= t) ? x : 0.f; });
 }
 
 // dA_tj = g_t . v_j + e_t for j <= t, else 0.
 __device__ void score_grads(float* dA, const float* Gs, const float* Vs, const float* ee, int ldv, int dv) {
-    for (int o = threadIdx.x; o < C * C; o += NT) {
-        const int t = o / C, j = o - t * C;
+    Tile tl(C);
+    tl.add(Gs, ldv, 1, Vs, 1, ldv, dv, 0, C);
+    tl.store(0, C, [&](int t, int j, float x) { dA[t * LDS + j] = (j <= t) ? x + ee[t] : 0.f; });
+}
+
+// ------------------------------------------------------------------ 64-token key-value sums
+// Record (bh, c) = [sum_t phi(k_t) v_t^T (d x dv row-major) | sum_t phi(k_t)] over the chunk.
+// Shared memory (float): Kf [C][d+1], Vs [C][dv+1].
+template <typename TI>
+__global__ void __launch_bounds__(NT) bwd_sums_kernel(BwdParams p) {
+    extern __shared__ float sm[];
+    const int d = p.d, dv = p.dv_dim;
+    const int ldq = d + 1, ldv = dv + 1;
+    const int c = blockIdx.x, bh = blockIdx.y;
+    const int64_t t0 = (int64_t)c * C;
+    const int nv = (int)min64(C, p.T - t0);
+    float* Kf = sm;
+    float* Vs = Kf + C * ldq;
+    const int64_t row0 = (int64_t)bh * p.T + t0;
+    load_rows(Kf, ldq, static_cast<const TI*>(p.k) + row0 * d, d, nv, true);
+    load_rows(Vs, ldv, static_cast<const TI*>(p.v) + row0 * dv, dv, nv, false);
+    __syncthreads();
+    float* rec = p.states + ((int64_t)bh * p.nch + c) * p.rec;
+    for (int r0 = 0; r0 < d; r0 += 64) {
+        Tile tl(dv);
+        tl.add(Kf, 1, ldq, Vs, ldv, 1, nv, r0, d);
+        tl.store(r0, d, [&](int i, int n, float x) { rec[i * dv + n] = x; });
+    }
+    for (int i = threadIdx.x; i < d; i += NT) {
         float acc = 0.f;
-        if (j <= t) {
-            const float* a = Gs + t * ldv;
-            const float* b = Vs + j * ldv;
-            for (int n = 0; n < dv; ++n) acc = fmaf(a[n], b[n], acc);
-            acc += ee[t];
-        }
-        dA[t * LDS + j] = acc;
+        for (int t = 0; t < nv; ++t) acc += Kf[t * ldq + i];
+        rec[(int64_t)d * dv + i] = acc;
     }
 }
 
 // ------------------------------------------------------------------ dq, G, E, chunk sums
 // Shared memory (float): Qf, Kf [C][d+1]; Vs, Os [C][dv+1]; Ms [d][dv+1]; Ss [C][C+1];
-// zs [d]; den, ee [C]. Os holds the numerator, then out, then g.
+// zs [d]; den, ee [C]. Os holds out, then g.
 template <typename TI>
 __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     extern __shared__ float sm[];
@@ -131,16 +233,22 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     float* den = zs + d;
     float* ee = den + C;
     const int64_t row0 = (int64_t)bh * p.T + t0;
-    const TI* q = static_cast<const TI*>(p.q) + row0 * d;
-    const TI* k = static_cast<const TI*>(p.k) + row0 * d;
-    const TI* v = static_cast<const TI*>(p.v) + row0 * dv;
     const TI* dout = static_cast<const TI*>(p.dout) + row0 * dv;
     TI* dq = static_cast<TI*>(p.dq) + row0 * d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // dout rows warp + 8r, columns lane + 32m of this thread's g/e pass, requested first
+    float dreg[C / 8][4];
+#pragma unroll
+    for (int r = 0; r < C / 8; ++r)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int t = warp + 8 * r, n = lane + 32 * m;
+            dreg[r][m] = (t < nv && n < dv) ? bld(dout + (int64_t)t * dv + n) : 0.f;
+        }
 
-    load_rows(Qf, ldq, q, d, nv, true);
-    load_rows(Kf, ldq, k, d, nv, true);
-    load_rows(Vs, ldv, v, dv, nv, false);
+    load_rows(Qf, ldq, static_cast<const TI*>(p.q) + row0 * d, d, nv, true);
+    load_rows(Kf, ldq, static_cast<const TI*>(p.k) + row0 * d, d, nv, true);
+    load_rows(Vs, ldv, static_cast<const TI*>(p.v) + row0 * dv, dv, nv, false);
     load_record(Ms, ldv, zs, p.states + ((int64_t)bh * p.nch + c) * p.rec, d, dv);
     __syncthreads();
     scores(Ss, Qf, Kf, ldq, d);
@@ -153,20 +261,22 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
         if (lane == 0) den[t] = s + p.eps;
     }
     __syncthreads();
-    for (int o = threadIdx.x; o < C * dv; o += NT) {  // out_t
-        const int t = o / dv, n = o - t * dv;
-        const float* a = Qf + t * ldq;
-        const float* s = Ss + t * LDS;
-        float acc = 0.f;
-        for (int i = 0; i < d; ++i) acc = fmaf(a[i], Ms[i * ldv + n], acc);
-        for (int j = 0; j <= t; ++j) acc = fmaf(s[j], Vs[j * ldv + n], acc);
-        Os[t * ldv + n] = (t < nv) ? acc / den[t] : 0.f;
+    {  // out_t = (phi(q_t)^T M + sum_j S_tj v_j) / D_t
+        Tile tl(dv);
+        tl.add(Qf, ldq, 1, Ms, ldv, 1, d, 0, C);
+        tl.add(Ss, LDS, 1, Vs, ldv, 1, C, 0, C);
+        tl.store(0, C, [&](int t, int n, float x) { Os[t * ldv + n] = (t < nv) ? x / den[t] : 0.f; });
     }
     __syncthreads();
-    for (int t = warp; t < C; t += NT / 32) {  // g_t and e_t
+#pragma unroll
+    for (int r = 0; r < C / 8; ++r) {  // g_t and e_t
+        const int t = warp + 8 * r;
         float s = 0.f;
-        for (int n = lane; n < dv; n += 32) {
-            const float g = (t < nv) ? bld(dout + (int64_t)t * dv + n) / den[t] : 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int n = lane + 32 * m;
+            if (n >= dv) break;
+            const float g = (t < nv) ? dreg[r][m] / den[t] : 0.f;
             s = fmaf(g, Os[t * ldv + n], s);
             Os[t * ldv + n] = g;
             if (t < nv) p.G[(row0 + t) * dv + n] = g;
@@ -180,24 +290,20 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     __syncthreads();
     score_grads(Ss, Os, Vs, ee, ldv, dv);
     __syncthreads();
-    for (int o = threadIdx.x; o < C * d; o += NT) {  // dq_t
-        const int t = o / d, i = o - t * d;
-        if (t >= nv) continue;
-        const float* g = Os + t * ldv;
-        const float* m = Ms + i * ldv;
-        const float* s = Ss + t * LDS;
-        float acc = ee[t] * zs[i];
-        for (int n = 0; n < dv; ++n) acc = fmaf(m[n], g[n], acc);
-        for (int j = 0; j <= t; ++j) acc = fmaf(s[j], Kf[j * ldq + i], acc);
-        bst(dq + (int64_t)t * d + i, acc * fminf(Qf[t * ldq + i], 1.f));
+    {  // dq_t = (M g_t + e_t z + sum_j dA_tj phi(k_j)) phi'(q_t)
+        Tile tl(d);
+        tl.add(Os, ldv, 1, Ms, 1, ldv, dv, 0, C);
+        tl.add(Ss, LDS, 1, Kf, ldq, 1, C, 0, C);
+        tl.store(0, nv, [&](int t, int i, float x) {
+            bst(dq + (int64_t)t * d + i, (x + ee[t] * zs[i]) * fminf(Qf[t * ldq + i], 1.f));
+        });
     }
     // chunk sums phi(Q)^T G and phi(Q)^T e (no barrier needed: Qf, Os, ee are unchanged)
     float* rv = p.rev + ((int64_t)bh * p.nch + c) * p.rec;
-    for (int o = threadIdx.x; o < d * dv; o += NT) {
-        const int i = o / dv, n = o - i * dv;
-        float acc = 0.f;
-        for (int t = 0; t < nv; ++t) acc = fmaf(Qf[t * ldq + i], Os[t * ldv + n], acc);
-        rv[o] = acc;
+    for (int r0 = 0; r0 < d; r0 += 64) {
+        Tile tl(dv);
+        tl.add(Qf, 1, ldq, Os, ldv, 1, nv, r0, d);
+        tl.store(r0, d, [&](int i, int n, float x) { rv[i * dv + n] = x; });
     }
     for (int i = threadIdx.x; i < d; i += NT) {
         float acc = 0.f;
@@ -208,12 +314,9 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
 
 // G and E rows of the chunk (rows >= nv become 0).
 __device__ void load_g(float* Gs, int ldv, float* ee, const BwdParams& p, int64_t row0, int nv) {
-    const int dv = p.dv_dim;
-    for (int idx = threadIdx.x; idx < C * dv; idx += NT) {
-        const int t = idx / dv, n = idx - t * dv;
-        Gs[t * ldv + n] = (t < nv) ? p.G[(row0 + t) * dv + n] : 0.f;
-    }
-    for (int t = threadIdx.x; t < C; t += NT) ee[t] = (t < nv) ? p.E[row0 + t] : 0.f;
+    load_rows(Gs, ldv, p.G + row0 * p.dv_dim, p.dv_dim, nv, false);
+    if (ee)
+        for (int t = threadIdx.x; t < C; t += NT) ee[t] = (t < nv) ? p.E[row0 + t] : 0.f;
 }
 
 // ------------------------------------------------------------------ dk
@@ -236,34 +339,27 @@ __global__ void __launch_bounds__(NT) bwd_dk_kernel(BwdParams p) {
     float* rs = dA + C * LDS;
     float* ee = rs + d;
     const int64_t row0 = (int64_t)bh * p.T + t0;
-    const TI* q = static_cast<const TI*>(p.q) + row0 * d;
-    const TI* k = static_cast<const TI*>(p.k) + row0 * d;
-    const TI* v = static_cast<const TI*>(p.v) + row0 * dv;
     TI* dk = static_cast<TI*>(p.dk) + row0 * d;
 
-    load_rows(Qf, ldq, q, d, nv, true);
-    load_rows(Kf, ldq, k, d, nv, true);
-    load_rows(Vs, ldv, v, dv, nv, false);
+    load_rows(Qf, ldq, static_cast<const TI*>(p.q) + row0 * d, d, nv, true);
+    load_rows(Kf, ldq, static_cast<const TI*>(p.k) + row0 * d, d, nv, true);
+    load_rows(Vs, ldv, static_cast<const TI*>(p.v) + row0 * dv, dv, nv, false);
     load_g(Gs, ldv, ee, p, row0, nv);
     load_record(Rs, ldv, rs, p.rev + ((int64_t)bh * p.nch + c) * p.rec, d, dv);
     __syncthreads();
     score_grads(dA, Gs, Vs, ee, ldv, dv);
     __syncthreads();
-    for (int o = threadIdx.x; o < C * d; o += NT) {
-        const int j = o / d, i = o - j * d;
-        if (j >= nv) continue;
-        const float* r = Rs + i * ldv;
-        const float* vj = Vs + j * ldv;
-        float acc = rs[i];
-        for (int n = 0; n < dv; ++n) acc = fmaf(r[n], vj[n], acc);
-        for (int t = j; t < nv; ++t) acc = fmaf(dA[t * LDS + j], Qf[t * ldq + i], acc);
-        bst(dk + (int64_t)j * d + i, acc * fminf(Kf[j * ldq + i], 1.f));
-    }
+    // dk_j = (sum_{t >= j} dA_tj phi(q_t) + R v_j + r) phi'(k_j)
+    Tile tl(d);
+    tl.add(dA, 1, LDS, Qf, ldq, 1, nv, 0, C);
+    tl.add(Vs, ldv, 1, Rs, 1, ldv, dv, 0, C);
+    tl.store(0, nv, [&](int j, int i, float x) {
+        bst(dk + (int64_t)j * d + i, (x + rs[i]) * fminf(Kf[j * ldq + i], 1.f));
+    });
 }
 
 // ------------------------------------------------------------------ dv
-// Shared memory (float): Qf, Kf [C][d+1]; Gs [C][dv+1]; Rs [d][dv+1]; Ss [C][C+1]; rs [d],
-// ee [C] (loaded with G, unused here).
+// Shared memory (float): Qf, Kf [C][d+1]; Gs [C][dv+1]; Rs [d][dv+1]; Ss [C][C+1]; rs [d].
 template <typename TI>
 __global__ void __launch_bounds__(NT) bwd_dv_kernel(BwdParams p) {
     extern __shared__ float sm[];
@@ -278,28 +374,21 @@ __global__ void __launch_bounds__(NT) bwd_dv_kernel(BwdParams p) {
     float* Rs = Gs + C * ldv;
     float* Ss = Rs + d * ldv;
     float* rs = Ss + C * LDS;
-    float* ee = rs + d;
     const int64_t row0 = (int64_t)bh * p.T + t0;
-    const TI* q = static_cast<const TI*>(p.q) + row0 * d;
-    const TI* k = static_cast<const TI*>(p.k) + row0 * d;
     TI* dvo = static_cast<TI*>(p.dv) + row0 * dv;
 
-    load_rows(Qf, ldq, q, d, nv, true);
-    load_rows(Kf, ldq, k, d, nv, true);
-    load_g(Gs, ldv, ee, p, row0, nv);
+    load_rows(Qf, ldq, static_cast<const TI*>(p.q) + row0 * d, d, nv, true);
+    load_rows(Kf, ldq, static_cast<const TI*>(p.k) + row0 * d, d, nv, true);
+    load_g(Gs, ldv, nullptr, p, row0, nv);
     load_record(Rs, ldv, rs, p.rev + ((int64_t)bh * p.nch + c) * p.rec, d, dv);
     __syncthreads();
     scores(Ss, Qf, Kf, ldq, d);
     __syncthreads();
-    for (int o = threadIdx.x; o < C * dv; o += NT) {
-        const int j = o / dv, n = o - j * dv;
-        if (j >= nv) continue;
-        const float* kj = Kf + j * ldq;
-        float acc = 0.f;
-        for (int i = 0; i < d; ++i) acc = fmaf(kj[i], Rs[i * ldv + n], acc);
-        for (int t = j; t < nv; ++t) acc = fmaf(Ss[t * LDS + j], Gs[t * ldv + n], acc);
-        bst(dvo + (int64_t)j * dv + n, acc);
-    }
+    // dv_j = sum_{t >= j} S_tj g_t + R^T phi(k_j)
+    Tile tl(dv);
+    tl.add(Ss, 1, LDS, Gs, ldv, 1, nv, 0, C);
+    tl.add(Kf, ldq, 1, Rs, ldv, 1, d, 0, C);
+    tl.store(0, nv, [&](int j, int n, float x) { bst(dvo + (int64_t)j * dv + n, x); });
 }
 
 // ------------------------------------------------------------------ exclusive scans over chunks
@@ -319,12 +408,12 @@ __global__ void __launch_bounds__(NT) scan_states_kernel(ScanParams p) {
     float* r = p.rec + (int64_t)bh * p.nch * p.len + e;
     auto at = [&](int i) -> float& { return r[(int64_t)(p.reverse ? p.nch - 1 - i : i) * p.len]; };
     int i = 0;
-    for (; i + 8 <= p.nch; i += 8) {  // eight loads in flight, then eight stores
-        float x[8];
+    for (; i + 16 <= p.nch; i += 16) {  // sixteen loads in flight, then sixteen stores
+        float x[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = at(i + u);
+        for (int u = 0; u < 16; ++u) x[u] = at(i + u);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
             at(i + u) = run;
             run += x[u];
         }
@@ -351,8 +440,9 @@ size_t dk_smem(int d, int dv) {
 }
 size_t dv_smem(int d, int dv) {
     return sizeof(float) * (2 * (size_t)C * (d + 1) + (size_t)C * (dv + 1) + (size_t)d * (dv + 1) +
-                            (size_t)C * LDS + d + C);
+                            (size_t)C * LDS + d);
 }
+size_t sums_smem(int d, int dv) { return sizeof(float) * ((size_t)C * (d + 1) + (size_t)C * (dv + 1)); }
 
 template <typename F32Fn, typename BF16Fn>
 cudaError_t launch_chunk_kernel(F32Fn f32, BF16Fn bf, const BwdParams& p, bool bf16, size_t smem, cudaStream_t s) {
@@ -386,6 +476,11 @@ cudaError_t launch_scan_states(const ScanParams& p, cudaStream_t s) {
     dim3 grid((unsigned)((p.len + NT - 1) / NT), p.BH);
     scan_states_kernel<<<grid, NT, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_sums(const BwdParams& p, bool bf16, cudaStream_t s) {
+    return launch_chunk_kernel(bwd_sums_kernel<float>, bwd_sums_kernel<__nv_bfloat16>, p, bf16,
+                               sums_smem(p.d, p.dv_dim), s);
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, cudaStream_t s) {

@@ -7,7 +7,8 @@ namespace la {
 constexpr int BWD_CH = 64;  // tokens per block of the backward
 
 // Workspace of the backward, in floats (each region starts on a 256-byte boundary):
-//   states [B*H][nch][rec]  state before chunk c (M at +0, z at +d*dv), float32
+//   states [B*H][nch][rec]  chunk sums, then (after the prefix scan) the state before
+//                           chunk c (M at +0, z at +d*dv), float32
 //   rev    [B*H][nch][rec]  chunk sums phi(Q_c)^T G_c and phi(Q_c)^T e_c; after the
 //                           reverse scan, the state gradient from every token after chunk c
 //   G      [B*H][T][dv]     g_t = dout_t / D_t
@@ -20,7 +21,7 @@ struct BwdParams {
     void* dq;
     void* dk;
     void* dv;
-    const float* states;
+    float* states;
     float* rev;
     float* G;
     float* E;
@@ -44,6 +45,7 @@ struct ScanParams {
 
 size_t bwd_workspace_floats(int64_t BH, int64_t T, int d, int dv, size_t* off_rev, size_t* off_G, size_t* off_E);
 cudaError_t launch_scan_states(const ScanParams& p, cudaStream_t s);
+cudaError_t launch_bwd_sums(const BwdParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dk(const BwdParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dv(const BwdParams& p, bool bf16, cudaStream_t s);

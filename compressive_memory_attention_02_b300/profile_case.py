@@ -2,9 +2,9 @@
 
   python -m compressive_memory_attention_02_b300.profile_case --mode fwd --B 2 --H 32 --T 2048 --repeat 3
 
-Modes: fwd (la_causal_fwd, training forward), prefill (la_prefill_state),
-decode (la_decode_step on a [B, H] batch of one-token streams with a random
-state). Inputs are the seeded synthetic N(0,1)*0.5 bf16 values; the call's
+Modes: fwd (la_causal_fwd, training forward), bwd (la_causal_bwd, training
+backward with dout ~ N(0,1)), prefill (la_prefill_state), decode (la_decode_step
+on a [B, H] batch of one-token streams with a random state). Inputs are the seeded synthetic N(0,1)*0.5 bf16 values; the call's
 workspace is registered before the first launch.
 """
 from __future__ import annotations
@@ -20,7 +20,7 @@ if ROOT not in sys.path:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--mode", default="fwd", choices=["fwd", "prefill", "decode"])
+    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "prefill", "decode"])
     ap.add_argument("--B", type=int, default=2)
     ap.add_argument("--H", type=int, default=32)
     ap.add_argument("--T", type=int, default=2048)
@@ -52,7 +52,14 @@ def main():
         v = bf(synthetic.normal(1, 2, (a.B, a.H, a.T, a.dv), 0.5, "bf16"))
         M = torch.empty(a.B, a.H, a.d, a.dv, device=dev)
         z = torch.empty(a.B, a.H, a.d, device=dev)
-        if a.mode == "fwd":
+        if a.mode == "bwd":
+            dout = bf(synthetic.normal(1, 7, (a.B, a.H, a.T, a.dv), 1.0, "bf16"))
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            la.ensure_workspace(la.la_causal_bwd_workspace_size(a.B, a.H, a.T, a.d, a.dv))
+            for _ in range(a.repeat):
+                la.la_causal_bwd(q, k, v, dout, None, None, None, None, dq, dk, dv, M, z, a.B, a.H, a.T, a.d, a.dv,
+                                 1e-6, la.LA_BF16)
+        elif a.mode == "fwd":
             out = torch.empty(a.B, a.H, a.T, a.dv, dtype=torch.bfloat16, device=dev)
             la.ensure_workspace(la.la_causal_fwd_workspace_size(a.B, a.H, a.T, a.d, a.dv, 64, la.LA_BF16))
             for _ in range(a.repeat):

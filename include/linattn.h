@@ -176,7 +176,7 @@ int la_decode_step(const void* q, const void* k, const void* v, void* out,
  * (M_t, z_t include token t; phi'(x) = 1 for x > 0, exp(x) otherwise; "o" is the
  * elementwise product). The forward quantities are recomputed from q, k, v, M_in, z_in
  * in float32; nothing from the forward call is needed.
- *   q, k [B,H,T,d], v, dout [B,H,T,dv]  dtype, contiguous, read
+ *   q, k [B,H,T,d], v, dout [B,H,T,dv]  dtype, contiguous, 16-byte aligned, read
  *   M_in, z_in        float32, read (NULL = zero initial state)
  *   dM_out, dz_out    float32 [B,H,d,dv] / [B,H,d], read (NULL = zero)
  *   dq, dk [B,H,T,d], dv [B,H,T,dv]  dtype, contiguous, written; must not alias an input

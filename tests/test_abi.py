@@ -93,3 +93,9 @@ def test_backward_workspace_size_and_host_checks():
     bad[8] = 16  # dq aliases q
     assert la.lib.la_causal_bwd(*bad, 1, 1, 64, 64, 64, 1e-6, 1, None) == la.LA_ERR_INVALID_ARG
     assert la.lib.la_causal_bwd(*args, 1, 1, 64, 64, 64, 1e-6, 3, None) == la.LA_ERR_UNSUPPORTED
+
+
+def test_backward_rejects_unaligned_inputs_on_host():
+    import compressive_memory_attention_02_b300 as la
+    args = [16, 32, 48, 72, None, None, None, None, 80, 96, 112, None, None]  # dout 8 bytes off
+    assert la.lib.la_causal_bwd(*args, 1, 1, 64, 64, 64, 1e-6, 1, None) == la.LA_ERR_INVALID_ARG
