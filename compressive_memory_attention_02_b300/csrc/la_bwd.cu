@@ -22,6 +22,8 @@
 // operand of the chunk in shared memory (tile rows padded by one float so that strided
 // reads by consecutive threads fall in distinct banks); its products run through Tile,
 // a register-tiled micro-kernel.
+#include <type_traits>
+
 #include "la_bwd.h"
 
 namespace la {
@@ -125,28 +127,35 @@ __device__ void load_record(float* Ms, int ld, float* zs, const float* rec, int 
 // Register-tiled product over shared-memory operands: out(r, n) += sum_k A(r, k) B(k, n)
 // with A(r, k) = A[r*ars + k*aks] and B(k, n) = B[k*bks + n*bns]. Thread (rg, cg) =
 // (tid / 16, tid % 16) owns rows r0 + rg + 16i (i < 4) and columns cg + 16j (j < 8, while
-// below N): per k it loads 4 + (up to) 8 operands for up to 32 multiply-adds. Rows past
-// R read row R-1 (in bounds) and are not stored.
+// below N): per k it loads 4 + (up to) 8 operands for up to 32 multiply-adds. With FX
+// (d and dv fixed at compile time, multiples of 64) every stride, N and K is a constant, so
+// the k loop unrolls into loads at constant offsets; otherwise rows past R read row R-1
+// (in bounds) and are not stored.
+template <bool FX>
 struct Tile {
     float acc[4][8];
     int rg, cg, nb;
-    __device__ explicit Tile(int N) : rg((int)threadIdx.x >> 4), cg((int)threadIdx.x & 15) {
-        nb = (N - cg + 15) >> 4;
+    __device__ __forceinline__ explicit Tile(int N) : rg((int)threadIdx.x >> 4), cg((int)threadIdx.x & 15) {
+        nb = FX ? (N >> 4) : ((N - cg + 15) >> 4);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
     }
-    __device__ void add(const float* A, int ars, int aks, const float* B, int bks, int bns, int K, int r0, int R) {
+    __device__ __forceinline__ void add(const float* A, int ars, int aks, const float* B, int bks, int bns, int K,
+                                        int r0, int R) {
         int ro[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) ro[i] = min(r0 + rg + 16 * i, R - 1) * ars;
+        for (int i = 0; i < 4; ++i) ro[i] = (FX ? r0 + rg + 16 * i : min(r0 + rg + 16 * i, R - 1)) * ars;
+        const float* pb = B + cg * bns;
+        constexpr int UNROLL = FX ? 4 : 1;  // runtime strides: keep the loop compact
+#pragma unroll UNROLL
         for (int k = 0; k < K; ++k) {
             float a[4], b[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) a[i] = A[ro[i] + k * aks];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) b[j] = (j < nb) ? B[k * bks + (cg + 16 * j) * bns] : 0.f;
+            for (int j = 0; j < 8; ++j) b[j] = (j < nb) ? pb[k * bks + 16 * j * bns] : 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -156,7 +165,7 @@ struct Tile {
     }
     // f(row, col, value) for every owned element with row < R
     template <class F>
-    __device__ void store(int r0, int R, F f) const {
+    __device__ __forceinline__ void store(int r0, int R, F f) const {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = r0 + rg + 16 * i;
@@ -169,15 +178,18 @@ struct Tile {
 };
 
 // S_tj = phi(q_t) . phi(k_j) for j <= t, else 0 (the C x C product, then the mask).
-__device__ void scores(float* Ss, const float* Qf, const float* Kf, int ldq, int d) {
-    Tile tl(C);
+template <bool FX>
+__device__ __forceinline__ void scores(float* Ss, const float* Qf, const float* Kf, int ldq, int d) {
+    Tile<FX> tl(C);
     tl.add(Qf, ldq, 1, Kf, 1, ldq, d, 0, C);
     tl.store(0, C, [&](int t, int j, float x) { Ss[t * LDS + j] = (j <= t) ? x : 0.f; });
 }
 
 // dA_tj = g_t . v_j + e_t for j <= t, else 0.
-__device__ void score_grads(float* dA, const float* Gs, const float* Vs, const float* ee, int ldv, int dv) {
-    Tile tl(C);
+template <bool FX>
+__device__ __forceinline__ void score_grads(float* dA, const float* Gs, const float* Vs, const float* ee, int ldv,
+                                            int dv) {
+    Tile<FX> tl(C);
     tl.add(Gs, ldv, 1, Vs, 1, ldv, dv, 0, C);
     tl.store(0, C, [&](int t, int j, float x) { dA[t * LDS + j] = (j <= t) ? x + ee[t] : 0.f; });
 }
@@ -185,10 +197,11 @@ __device__ void score_grads(float* dA, const float* Gs, const float* Vs, const f
 // ------------------------------------------------------------------ 64-token key-value sums
 // Record (bh, c) = [sum_t phi(k_t) v_t^T (d x dv row-major) | sum_t phi(k_t)] over the chunk.
 // Shared memory (float): Kf [C][d+1], Vs [C][dv+1].
-template <typename TI>
+template <typename TI, int DT, int DVT>
 __global__ void __launch_bounds__(NT) bwd_sums_kernel(BwdParams p) {
     extern __shared__ float sm[];
-    const int d = p.d, dv = p.dv_dim;
+    constexpr bool FX = DT > 0;  // d, dv fixed at compile time
+    const int d = FX ? DT : p.d, dv = FX ? DVT : p.dv_dim;
     const int ldq = d + 1, ldv = dv + 1;
     const int c = blockIdx.x, bh = blockIdx.y;
     const int64_t t0 = (int64_t)c * C;
@@ -201,8 +214,8 @@ __global__ void __launch_bounds__(NT) bwd_sums_kernel(BwdParams p) {
     __syncthreads();
     float* rec = p.states + ((int64_t)bh * p.nch + c) * p.rec;
     for (int r0 = 0; r0 < d; r0 += 64) {
-        Tile tl(dv);
-        tl.add(Kf, 1, ldq, Vs, ldv, 1, nv, r0, d);
+        Tile<FX> tl(dv);
+        tl.add(Kf, 1, ldq, Vs, ldv, 1, FX ? C : nv, r0, d);
         tl.store(r0, d, [&](int i, int n, float x) { rec[i * dv + n] = x; });
     }
     for (int i = threadIdx.x; i < d; i += NT) {
@@ -215,10 +228,11 @@ __global__ void __launch_bounds__(NT) bwd_sums_kernel(BwdParams p) {
 // ------------------------------------------------------------------ dq, G, E, chunk sums
 // Shared memory (float): Qf, Kf [C][d+1]; Vs, Os [C][dv+1]; Ms [d][dv+1]; Ss [C][C+1];
 // zs [d]; den, ee [C]. Os holds out, then g.
-template <typename TI>
+template <typename TI, int DT, int DVT>
 __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     extern __shared__ float sm[];
-    const int d = p.d, dv = p.dv_dim;
+    constexpr bool FX = DT > 0;  // d, dv fixed at compile time
+    const int d = FX ? DT : p.d, dv = FX ? DVT : p.dv_dim;
     const int ldq = d + 1, ldv = dv + 1;
     const int c = blockIdx.x, bh = blockIdx.y;
     const int64_t t0 = (int64_t)c * C;
@@ -251,7 +265,7 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     load_rows(Vs, ldv, static_cast<const TI*>(p.v) + row0 * dv, dv, nv, false);
     load_record(Ms, ldv, zs, p.states + ((int64_t)bh * p.nch + c) * p.rec, d, dv);
     __syncthreads();
-    scores(Ss, Qf, Kf, ldq, d);
+    scores<FX>(Ss, Qf, Kf, ldq, d);
     __syncthreads();
     for (int t = warp; t < C; t += NT / 32) {  // D_t
         float s = 0.f;
@@ -262,7 +276,7 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     }
     __syncthreads();
     {  // out_t = (phi(q_t)^T M + sum_j S_tj v_j) / D_t
-        Tile tl(dv);
+        Tile<FX> tl(dv);
         tl.add(Qf, ldq, 1, Ms, ldv, 1, d, 0, C);
         tl.add(Ss, LDS, 1, Vs, ldv, 1, C, 0, C);
         tl.store(0, C, [&](int t, int n, float x) { Os[t * ldv + n] = (t < nv) ? x / den[t] : 0.f; });
@@ -288,10 +302,10 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
         }
     }
     __syncthreads();
-    score_grads(Ss, Os, Vs, ee, ldv, dv);
+    score_grads<FX>(Ss, Os, Vs, ee, ldv, dv);
     __syncthreads();
     {  // dq_t = (M g_t + e_t z + sum_j dA_tj phi(k_j)) phi'(q_t)
-        Tile tl(d);
+        Tile<FX> tl(d);
         tl.add(Os, ldv, 1, Ms, 1, ldv, dv, 0, C);
         tl.add(Ss, LDS, 1, Kf, ldq, 1, C, 0, C);
         tl.store(0, nv, [&](int t, int i, float x) {
@@ -301,8 +315,8 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     // chunk sums phi(Q)^T G and phi(Q)^T e (no barrier needed: Qf, Os, ee are unchanged)
     float* rv = p.rev + ((int64_t)bh * p.nch + c) * p.rec;
     for (int r0 = 0; r0 < d; r0 += 64) {
-        Tile tl(dv);
-        tl.add(Qf, 1, ldq, Os, ldv, 1, nv, r0, d);
+        Tile<FX> tl(dv);
+        tl.add(Qf, 1, ldq, Os, ldv, 1, FX ? C : nv, r0, d);
         tl.store(r0, d, [&](int i, int n, float x) { rv[i * dv + n] = x; });
     }
     for (int i = threadIdx.x; i < d; i += NT) {
@@ -322,10 +336,11 @@ __device__ void load_g(float* Gs, int ldv, float* ee, const BwdParams& p, int64_
 // ------------------------------------------------------------------ dk
 // Shared memory (float): Qf, Kf [C][d+1]; Vs, Gs [C][dv+1]; Rs [d][dv+1]; dA [C][C+1];
 // rs [d]; ee [C].
-template <typename TI>
+template <typename TI, int DT, int DVT>
 __global__ void __launch_bounds__(NT) bwd_dk_kernel(BwdParams p) {
     extern __shared__ float sm[];
-    const int d = p.d, dv = p.dv_dim;
+    constexpr bool FX = DT > 0;  // d, dv fixed at compile time
+    const int d = FX ? DT : p.d, dv = FX ? DVT : p.dv_dim;
     const int ldq = d + 1, ldv = dv + 1;
     const int c = blockIdx.x, bh = blockIdx.y;
     const int64_t t0 = (int64_t)c * C;
@@ -347,11 +362,11 @@ __global__ void __launch_bounds__(NT) bwd_dk_kernel(BwdParams p) {
     load_g(Gs, ldv, ee, p, row0, nv);
     load_record(Rs, ldv, rs, p.rev + ((int64_t)bh * p.nch + c) * p.rec, d, dv);
     __syncthreads();
-    score_grads(dA, Gs, Vs, ee, ldv, dv);
+    score_grads<FX>(dA, Gs, Vs, ee, ldv, dv);
     __syncthreads();
     // dk_j = (sum_{t >= j} dA_tj phi(q_t) + R v_j + r) phi'(k_j)
-    Tile tl(d);
-    tl.add(dA, 1, LDS, Qf, ldq, 1, nv, 0, C);
+    Tile<FX> tl(d);
+    tl.add(dA, 1, LDS, Qf, ldq, 1, FX ? C : nv, 0, C);
     tl.add(Vs, ldv, 1, Rs, 1, ldv, dv, 0, C);
     tl.store(0, nv, [&](int j, int i, float x) {
         bst(dk + (int64_t)j * d + i, (x + rs[i]) * fminf(Kf[j * ldq + i], 1.f));
@@ -360,10 +375,11 @@ __global__ void __launch_bounds__(NT) bwd_dk_kernel(BwdParams p) {
 
 // ------------------------------------------------------------------ dv
 // Shared memory (float): Qf, Kf [C][d+1]; Gs [C][dv+1]; Rs [d][dv+1]; Ss [C][C+1]; rs [d].
-template <typename TI>
+template <typename TI, int DT, int DVT>
 __global__ void __launch_bounds__(NT) bwd_dv_kernel(BwdParams p) {
     extern __shared__ float sm[];
-    const int d = p.d, dv = p.dv_dim;
+    constexpr bool FX = DT > 0;  // d, dv fixed at compile time
+    const int d = FX ? DT : p.d, dv = FX ? DVT : p.dv_dim;
     const int ldq = d + 1, ldv = dv + 1;
     const int c = blockIdx.x, bh = blockIdx.y;
     const int64_t t0 = (int64_t)c * C;
@@ -382,11 +398,11 @@ __global__ void __launch_bounds__(NT) bwd_dv_kernel(BwdParams p) {
     load_g(Gs, ldv, nullptr, p, row0, nv);
     load_record(Rs, ldv, rs, p.rev + ((int64_t)bh * p.nch + c) * p.rec, d, dv);
     __syncthreads();
-    scores(Ss, Qf, Kf, ldq, d);
+    scores<FX>(Ss, Qf, Kf, ldq, d);
     __syncthreads();
     // dv_j = sum_{t >= j} S_tj g_t + R^T phi(k_j)
-    Tile tl(dv);
-    tl.add(Ss, 1, LDS, Gs, ldv, 1, nv, 0, C);
+    Tile<FX> tl(dv);
+    tl.add(Ss, 1, LDS, Gs, ldv, 1, FX ? C : nv, 0, C);
     tl.add(Kf, ldq, 1, Rs, ldv, 1, d, 0, C);
     tl.store(0, nv, [&](int j, int n, float x) { bst(dvo + (int64_t)j * dv + n, x); });
 }
@@ -478,21 +494,44 @@ cudaError_t launch_scan_states(const ScanParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Calls f with the compile-time shape (D, DV) of the specialised kernels, or (0, 0).
+template <class F>
+cudaError_t by_shape(const BwdParams& p, F f) {
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    if (p.d == 64 && p.dv_dim == 64) return f(I64{}, I64{});
+    if (p.d == 128 && p.dv_dim == 128) return f(I128{}, I128{});
+    if (p.d == 64 && p.dv_dim == 128) return f(I64{}, I128{});
+    if (p.d == 128 && p.dv_dim == 64) return f(I128{}, I64{});
+    return f(std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{});
+}
+
 cudaError_t launch_bwd_sums(const BwdParams& p, bool bf16, cudaStream_t s) {
-    return launch_chunk_kernel(bwd_sums_kernel<float>, bwd_sums_kernel<__nv_bfloat16>, p, bf16,
-                               sums_smem(p.d, p.dv_dim), s);
+    return by_shape(p, [&](auto D, auto DV) {
+        return launch_chunk_kernel(bwd_sums_kernel<float, D(), DV()>, bwd_sums_kernel<__nv_bfloat16, D(), DV()>, p,
+                                   bf16, sums_smem(p.d, p.dv_dim), s);
+    });
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, cudaStream_t s) {
-    return launch_chunk_kernel(bwd_dq_kernel<float>, bwd_dq_kernel<__nv_bfloat16>, p, bf16, dq_smem(p.d, p.dv_dim), s);
+    return by_shape(p, [&](auto D, auto DV) {
+        return launch_chunk_kernel(bwd_dq_kernel<float, D(), DV()>, bwd_dq_kernel<__nv_bfloat16, D(), DV()>, p, bf16,
+                                   dq_smem(p.d, p.dv_dim), s);
+    });
 }
 
 cudaError_t launch_bwd_dk(const BwdParams& p, bool bf16, cudaStream_t s) {
-    return launch_chunk_kernel(bwd_dk_kernel<float>, bwd_dk_kernel<__nv_bfloat16>, p, bf16, dk_smem(p.d, p.dv_dim), s);
+    return by_shape(p, [&](auto D, auto DV) {
+        return launch_chunk_kernel(bwd_dk_kernel<float, D(), DV()>, bwd_dk_kernel<__nv_bfloat16, D(), DV()>, p, bf16,
+                                   dk_smem(p.d, p.dv_dim), s);
+    });
 }
 
 cudaError_t launch_bwd_dv(const BwdParams& p, bool bf16, cudaStream_t s) {
-    return launch_chunk_kernel(bwd_dv_kernel<float>, bwd_dv_kernel<__nv_bfloat16>, p, bf16, dv_smem(p.d, p.dv_dim), s);
+    return by_shape(p, [&](auto D, auto DV) {
+        return launch_chunk_kernel(bwd_dv_kernel<float, D(), DV()>, bwd_dv_kernel<__nv_bfloat16, D(), DV()>, p, bf16,
+                                   dv_smem(p.d, p.dv_dim), s);
+    });
 }
 
 }  // namespace la
