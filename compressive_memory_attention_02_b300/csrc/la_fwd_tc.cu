@@ -403,31 +403,49 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             tc_fence_after();
             uint8_t* prow = sm + L::PT + buf * ATOM + t * 128;
             uint64_t rowsum2 = 0;  // (even keys, odd keys) partial sums
-#pragma unroll 1
-            for (int qt = 0; qt < 4; ++qt) {  // keys 16qt .. 16qt+15
-                uint32_t x[16];
-                tmem_ld16(tmem + tm_s(buf) + lane_base + 16 * qt, x);
+            const uint32_t srow = tmem + tm_s(buf) + lane_base;
+            // keys 32h .. 32h+31 of the row from x[0..32): P as bf16 into the swizzled tile, row sum
+            auto half = [&](const uint32_t* x, int h, bool diag) {
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int c0 = 32 * h + 8 * g8 + 2 * jj;
+                        float s0 = __uint_as_float(x[8 * g8 + 2 * jj]);
+                        float s1 = __uint_as_float(x[8 * g8 + 2 * jj + 1]);
+                        if (diag) {
+                            s0 = (c0 <= t) ? s0 : 0.f;
+                            s1 = (c0 + 1 <= t) ? s1 : 0.f;
+                        }
+                        pk[jj] = pack_bf16(s0, s1);
+                        rowsum2 = f2_add(rowsum2, f2_pack(bf16lo(pk[jj]), bf16hi(pk[jj])));
+                    }
+                    *reinterpret_cast<uint4*>(prow + (((4 * h + g8) ^ (t & 7)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            };
+            uint32_t zq;
+            if (q == 0) {  // rows 0-31: keys 32-63 all lie after the row
+                uint32_t x[32];
+                tmem_ld32(srow, x);
+                zq = tmem_ld1(srow + 64);
                 tmem_wait_ld();
-                uint32_t pk[8];
+                half(x, 0, true);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int c0 = 16 * qt + 2 * jj;
-                    const float s0 = (c0 <= t) ? __uint_as_float(x[2 * jj]) : 0.f;
-                    const float s1 = (c0 + 1 <= t) ? __uint_as_float(x[2 * jj + 1]) : 0.f;
-                    pk[jj] = pack_bf16(s0, s1);
-                    rowsum2 = f2_add(rowsum2, f2_pack(bf16lo(pk[jj]), bf16hi(pk[jj])));
-                }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int c2 = 2 * qt + u;
-                    *reinterpret_cast<uint4*>(prow + ((c2 ^ (t & 7)) << 4)) =
-                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                }
+                for (int g8 = 4; g8 < 8; ++g8)
+                    *reinterpret_cast<uint4*>(prow + ((g8 ^ (t & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            } else {       // rows 32-63: keys 0-31 all lie before the row
+                uint32_t x[32];
+                tmem_ld32(srow, x);
+                tmem_wait_ld();
+                half(x, 0, false);
+                tmem_ld32(srow + 32, x);
+                zq = tmem_ld1(srow + 64);
+                tmem_wait_ld();
+                half(x, 1, true);
             }
-            uint32_t zc[16];
-            tmem_ld16(tmem + tm_s(buf) + lane_base + 64, zc);
-            tmem_wait_ld();
-            rden[buf * 64 + t] = 1.f / (__uint_as_float(zc[0]) + (f2_lo(rowsum2) + f2_hi(rowsum2)) + p.eps);
+            rden[buf * 64 + t] = 1.f / (__uint_as_float(zq) + (f2_lo(rowsum2) + f2_hi(rowsum2)) + p.eps);
             tc_fence_before();
             fence_proxy_async_smem();
             named_bar_sync(2, 64);

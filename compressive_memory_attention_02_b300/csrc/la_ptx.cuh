@@ -224,6 +224,13 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
                  : "r"(taddr));
 }
 
+// 32 lanes x 1 column of 32-bit: thread i gets lane (base_lane + i), column col
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+
 // 32 lanes x 16 columns of 32-bit: thread i gets lane (base_lane + i), columns col..col+15
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
     asm volatile(
