@@ -131,10 +131,12 @@ __device__ void load_record(float* Ms, int ld, float* zs, const float* rec, int 
 // (d and dv fixed at compile time, multiples of 64) every stride, N and K is a constant, so
 // the k loop unrolls into loads at constant offsets; otherwise rows past R read row R-1
 // (in bounds) and are not stored.
-template <bool FX>
+template <bool FX, bool BLK = false>
 struct Tile {
     float acc[4][8];
     int rg, cg, nb;
+    // row i of this thread (before r0): rows rg + 16i, or with BLK the four rows 4rg .. 4rg+3
+    __device__ __forceinline__ int row(int i) const { return BLK ? 4 * rg + i : rg + 16 * i; }
     __device__ __forceinline__ explicit Tile(int N) : rg((int)threadIdx.x >> 4), cg((int)threadIdx.x & 15) {
         nb = FX ? (N >> 4) : ((N - cg + 15) >> 4);
 #pragma unroll
@@ -146,11 +148,35 @@ struct Tile {
                                         int r0, int R) {
         int ro[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) ro[i] = (FX ? r0 + rg + 16 * i : min(r0 + rg + 16 * i, R - 1)) * ars;
+        for (int i = 0; i < 4; ++i) ro[i] = (FX ? r0 + row(i) : min(r0 + row(i), R - 1)) * ars;
         const float* pb = B + cg * bns;
         constexpr int UNROLL = FX ? 4 : 1;  // runtime strides: keep the loop compact
 #pragma unroll UNROLL
         for (int k = 0; k < K; ++k) {
+            float a[4], b[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = A[ro[i] + k * aks];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) b[j] = (j < nb) ? pb[k * bks + 16 * j * bns] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < nb) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+    }
+    // The same product over k in [kb, ke) only, for a C-row product (r0 = 0, R = C): with BLK,
+    // a causal mask bounds k per thread (keys up to the thread's last row, or queries from
+    // its first row on) and the masked terms are skipped instead of multiplied by zero.
+    __device__ __forceinline__ void add_range(const float* A, int ars, int aks, const float* B, int bks, int bns,
+                                              int kb, int ke) {
+        int ro[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ro[i] = row(i) * ars;
+        const float* pb = B + cg * bns;
+        constexpr int UNROLL = FX ? 4 : 1;
+#pragma unroll UNROLL
+        for (int k = kb; k < ke; ++k) {
             float a[4], b[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) a[i] = A[ro[i] + k * aks];
@@ -168,7 +194,7 @@ struct Tile {
     __device__ __forceinline__ void store(int r0, int R, F f) const {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int r = r0 + rg + 16 * i;
+            const int r = r0 + row(i);
             if (r >= R) continue;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -276,9 +302,9 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     }
     __syncthreads();
     {  // out_t = (phi(q_t)^T M + sum_j S_tj v_j) / D_t
-        Tile<FX> tl(dv);
+        Tile<FX, true> tl(dv);
         tl.add(Qf, ldq, 1, Ms, ldv, 1, d, 0, C);
-        tl.add(Ss, LDS, 1, Vs, ldv, 1, C, 0, C);
+        tl.add_range(Ss, LDS, 1, Vs, ldv, 1, 0, 4 * tl.rg + 4);  // keys j <= t
         tl.store(0, C, [&](int t, int n, float x) { Os[t * ldv + n] = (t < nv) ? x / den[t] : 0.f; });
     }
     __syncthreads();
@@ -305,9 +331,9 @@ __global__ void __launch_bounds__(NT) bwd_dq_kernel(BwdParams p) {
     score_grads<FX>(Ss, Os, Vs, ee, ldv, dv);
     __syncthreads();
     {  // dq_t = (M g_t + e_t z + sum_j dA_tj phi(k_j)) phi'(q_t)
-        Tile<FX> tl(d);
+        Tile<FX, true> tl(d);
         tl.add(Os, ldv, 1, Ms, 1, ldv, dv, 0, C);
-        tl.add(Ss, LDS, 1, Kf, ldq, 1, C, 0, C);
+        tl.add_range(Ss, LDS, 1, Kf, ldq, 1, 0, 4 * tl.rg + 4);  // keys j <= t
         tl.store(0, nv, [&](int t, int i, float x) {
             bst(dq + (int64_t)t * d + i, (x + ee[t] * zs[i]) * fminf(Qf[t * ldq + i], 1.f));
         });
@@ -365,8 +391,8 @@ __global__ void __launch_bounds__(NT) bwd_dk_kernel(BwdParams p) {
     score_grads<FX>(dA, Gs, Vs, ee, ldv, dv);
     __syncthreads();
     // dk_j = (sum_{t >= j} dA_tj phi(q_t) + R v_j + r) phi'(k_j)
-    Tile<FX> tl(d);
-    tl.add(dA, 1, LDS, Qf, ldq, 1, FX ? C : nv, 0, C);
+    Tile<FX, true> tl(d);
+    tl.add_range(dA, 1, LDS, Qf, ldq, 1, 4 * tl.rg, FX ? C : nv);  // queries t >= j
     tl.add(Vs, ldv, 1, Rs, 1, ldv, dv, 0, C);
     tl.store(0, nv, [&](int j, int i, float x) {
         bst(dk + (int64_t)j * d + i, (x + rs[i]) * fminf(Kf[j * ldq + i], 1.f));
@@ -401,8 +427,8 @@ __global__ void __launch_bounds__(NT) bwd_dv_kernel(BwdParams p) {
     scores<FX>(Ss, Qf, Kf, ldq, d);
     __syncthreads();
     // dv_j = sum_{t >= j} S_tj g_t + R^T phi(k_j)
-    Tile<FX> tl(dv);
-    tl.add(Ss, 1, LDS, Gs, ldv, 1, FX ? C : nv, 0, C);
+    Tile<FX, true> tl(dv);
+    tl.add_range(Ss, 1, LDS, Gs, ldv, 1, 4 * tl.rg, FX ? C : nv);  // queries t >= j
     tl.add(Kf, ldq, 1, Rs, ldv, 1, d, 0, C);
     tl.store(0, nv, [&](int j, int n, float x) { bst(dvo + (int64_t)j * dv + n, x); });
 }
