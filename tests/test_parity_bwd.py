@@ -111,6 +111,20 @@ def test_bf16_training_workload_sampled_heads():
         _compare(head, ref, TOL_BF16)
 
 
+def test_bf16_segment_call_shape_sampled_heads():
+    """One segment call of the segmented workload's shape (B=2, H=32, T=2048, d=dv=128) with a
+    carried-in state and state gradients; three heads checked against the oracle."""
+    B, H, T, d, dv = 2, 32, 2048, 128, 128
+    q, k, v, dout = _inputs(700, B, H, T, d, dv, "bf16", 0.5)
+    M0, z0 = rand_state(701, B, H, d, dv)
+    dM, dz = _state_grads(702, B, H, d, dv)
+    got = bwd(to_dev(q), to_dev(k), to_dev(v), to_dev(dout), to_dev(M0), to_dev(z0), to_dev(dM), to_dev(dz))
+    for b, h in ((0, 0), (1, 17), (1, 31)):
+        sl = lambda a: np.ascontiguousarray(a[b:b + 1, h:h + 1])
+        ref = oracle.causal_bwd(sl(q), sl(k), sl(v), _values(sl(dout)), sl(M0), sl(z0), sl(dM), sl(dz))
+        _compare([g[b:b + 1, h:h + 1] for g in got], ref, TOL_BF16)
+
+
 # ------------------------------------------------------------------ properties and the ABI
 
 def test_segment_backwards_chain_through_state_gradients():
