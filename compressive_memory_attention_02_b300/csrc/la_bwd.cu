@@ -126,8 +126,9 @@ __device__ void load_record(float* Ms, int ld, float* zs, const float* rec, int 
 
 // Register-tiled product over shared-memory operands: out(r, n) += sum_k A(r, k) B(k, n)
 // with A(r, k) = A[r*ars + k*aks] and B(k, n) = B[k*bks + n*bns]. Thread (rg, cg) =
-// (tid / 16, tid % 16) owns rows r0 + rg + 16i (i < 4) and columns cg + 16j (j < 8, while
-// below N): per k it loads 4 + (up to) 8 operands for up to 32 multiply-adds. With FX
+// (tid / 16, tid % 16) owns rows r0 + rg + 16i (i < 4; with BLK the four consecutive rows
+// r0 + 4rg + i) and columns cg + 16j (j < 8, while below N): per k it loads 4 + (up to) 8
+// operands for up to 32 multiply-adds. With FX
 // (d and dv fixed at compile time, multiples of 64) every stride, N and K is a constant, so
 // the k loop unrolls into loads at constant offsets; otherwise rows past R read row R-1
 // (in bounds) and are not stored.
