@@ -76,7 +76,7 @@ enum {
  *   M_in,z_in  initial state [B,H,d,dv] / [B,H,d] float32, read; NULL = zero state
  *   M_out,z_out final state, written; NULL = not written; M_out may equal M_in
  *              (and z_out z_in): the update is then in place
- *   chunk    intra-chunk block length; eps > 0 added to every denominator. */
+ *   chunk    intra-chunk block length; eps >= 0 added to every denominator. */
 int la_causal_fwd(const void* q, const void* k, const void* v, void* out,
                   const float* M_in, const float* z_in, float* M_out, float* z_out,
                   int B, int H, int64_t T, int d, int dv, int chunk, float eps,
