@@ -181,3 +181,23 @@ def test_backward_pins_pass_for_the_oracle():
 @pytest.mark.parametrize("mutation", [11, 12, 13, 14, 15, 16])
 def test_planted_backward_mistakes_are_caught(mutation):
     assert not _bwd_pins_pass(mutation)
+
+
+def test_backward_hand_worked_example():
+    """tests/golden/hand_worked_bwd.json: T = 2, d = dv = 1, eps = 1, values derived by hand."""
+    import json
+    import os
+    from fractions import Fraction
+    with open(os.path.join(os.path.dirname(__file__), "golden", "hand_worked_bwd.json")) as f:
+        g = json.load(f)
+    x = g["inputs"]
+    arr = lambda a, n: np.array(a, dtype=np.float32).reshape(1, 1, 2, n)
+    q, k, v = arr(x["q"], 1), arr(x["k"], 1), arr(x["v"], 1)
+    dout = np.array(x["dout"], dtype=np.float64).reshape(1, 1, 2, 1)
+    dq, dk, dvv, dM, dz = oracle.causal_bwd(q, k, v, dout, eps=x["eps"])
+    fr = lambda s: float(Fraction(s))
+    e = g["expected"]
+    for got, want in ((dq, e["dq"]), (dk, e["dk"]), (dvv, e["dv"])):
+        assert np.allclose(got.reshape(-1), [fr(s) for s in want], rtol=1e-14, atol=0)
+    assert abs(dM.item() - fr(e["dM_in"])) <= 1e-14 * abs(fr(e["dM_in"]))
+    assert abs(dz.item() - fr(e["dz_in"])) <= 1e-14 * abs(fr(e["dz_in"]))
