@@ -1,8 +1,9 @@
 """Pins for the oracle's training backward (oracle.causal_bwd). Each check compares
-it with something other than itself: central finite differences of a float64
-forward written out in this file, float64 autograd of the masked all-pairs form,
-the single-token closed form, and the chaining of segment backwards through the
-state gradient. test_planted_backward_mistakes_are_caught shows that each of six
+it with something other than itself: a hand-worked example with exact rational values
+(tests/golden/hand_worked_bwd.json), central finite differences of a float64 forward
+written out in this file, float64 autograd of the masked all-pairs form, the
+single-token closed form, and the chaining of segment backwards through the state
+gradient. test_planted_backward_mistakes_are_caught shows that each of six
 planted mistakes (a dropped normaliser term, an off-by-one state, an ignored state
 gradient, a token missing from its own key gradient, a wrong phi', a transposed
 state) fails at least one of them."""
