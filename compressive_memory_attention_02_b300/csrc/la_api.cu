@@ -22,6 +22,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kSmemLimit = 227 * 1024;
 
 struct DeviceState {
+    unsigned long long ctx_id = 0;  // context the cached addresses belong to (0: none yet)
     int* status = nullptr;
     void* ws = nullptr;
     size_t ws_bytes = 0;
@@ -30,16 +31,54 @@ struct DeviceState {
 static DeviceState g_dev[kMaxDevices];
 static std::mutex g_mu;
 
+// Driver calls reached through the runtime's entry-point query (the library links
+// only the runtime).
+template <typename F>
+static F driver_fn(const char* name, int version) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<F>(p);
+    return nullptr;
+}
+
+int current_context_id(unsigned long long* id) {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        get_current = driver_fn<GetCurrent>("cuCtxGetCurrent", 4000);
+        get_id = driver_fn<GetId>("cuCtxGetId", 12000);
+    });
+    if (!get_current || !get_id) return LA_ERR_CUDA;
+    // a runtime call first, so that the device's primary context is current on this thread
+    if (cudaFree(nullptr) != cudaSuccess) return LA_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+// Per-device state, looked up again whenever the current context is not the one the
+// cached addresses were taken in (after cudaDeviceReset the module is loaded anew
+// and its device variables may live elsewhere; a registered workspace belonged to
+// the old context and is dropped).
 static int current_device(DeviceState** st) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != LA_OK) return LA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState& s = g_dev[dev];
-    if (!s.status) {
+    if (s.ctx_id != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return LA_ERR_CUDA;
+        s = DeviceState{};
         s.status = static_cast<int*>(p);
         cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        s.ctx_id = ctx;
     }
     *st = &s;
     return LA_OK;
@@ -55,14 +94,7 @@ int device_status_word(int** status) {
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
+    std::call_once(once, [] { fn = driver_fn<PFN_cuTensorMapEncodeTiled_v12000>("cuTensorMapEncodeTiled", 12000); });
     return fn;
 }
 
@@ -275,6 +307,8 @@ struct PrefillPlan {
     size_t final_bytes = 0;   // final state when M_out / z_out are not given
 };
 
+static bool aligned16_or_null(const void* p) { return !p || aligned16(p); }
+
 static PrefillPlan plan_prefill(int B, int H, int64_t T, int d, int dv, int segment, la_dtype dtype) {
     PrefillPlan pl;
     const int64_t BH = (int64_t)B * H;
@@ -289,6 +323,14 @@ static PrefillPlan plan_prefill(int B, int H, int64_t T, int d, int dv, int segm
     return pl;
 }
 
+size_t prefill_scratch_bytes(int B, int H, int64_t T, int d, int dv, int segment, la_dtype dtype,
+                             const void* out_last, const float* M_out, const float* z_out) {
+    if (!out_last && !M_out && !z_out) return 0;  // nothing requested: the call returns at once
+    const PrefillPlan pl = plan_prefill(B, H, T, d, dv, segment, dtype);
+    const bool need_final = out_last && (!M_out || !z_out);
+    return pl.parts_bytes + (need_final ? pl.final_bytes : 0);
+}
+
 int prefill_impl(const void* q, const void* k, const void* v, void* out_last, const float* M_in,
                         const float* z_in, float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv,
                         int segment, float eps, la_dtype dtype, const int64_t* strides, void* ws, size_t ws_bytes,
@@ -298,6 +340,10 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
     if (B <= 0 || H <= 0 || T <= 0 || segment < 0 || !(eps >= 0.f)) return LA_ERR_INVALID_ARG;
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
     if (!shape_ok(d, dv)) return LA_ERR_UNSUPPORTED;
+    // the ordered reduce of the parts moves the state in 16-byte vectors
+    if (!aligned16_or_null(M_in) || !aligned16_or_null(z_in) || !aligned16_or_null(M_out) ||
+        !aligned16_or_null(z_out))
+        return LA_ERR_INVALID_ARG;
     if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return LA_ERR_WORKSPACE;
     Strides st = strides ? from_array(strides) : contiguous(H, T, d, dv);
     if (!strides_valid(st, d, dv, false)) return LA_ERR_INVALID_ARG;
@@ -312,7 +358,7 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
     PrefillPlan pl = plan_prefill(B, H, T, d, dv, segment, dtype);
     if (pl.tc && !(aligned16(k) && aligned16(v) && strides_tma(st, false))) pl.tc = false;
     const bool need_final = out_last && (!M_out || !z_out);
-    const size_t need = pl.parts_bytes + (need_final ? pl.final_bytes : 0);
+    const size_t need = prefill_scratch_bytes(B, H, T, d, dv, segment, dtype, out_last, M_out, z_out);
     if (ws_bytes < need || !ws) {
         // no (or too little) scratch: one part per head, state straight into M_out/z_out
         pl.nparts = 1;

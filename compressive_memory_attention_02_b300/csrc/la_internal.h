@@ -133,6 +133,16 @@ cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUte
 // Device address of the current device's status word (la_api.cu).
 int device_status_word(int** status);
 
+// Unique id (cuCtxGetId) of the context current on this thread, after making the
+// current device's primary context current; LA_ERR_CUDA if it cannot be had.
+int current_context_id(unsigned long long* id);
+
+// Scratch bytes the prefill uses for this call when the scratch is large enough for its
+// fastest schedule: the per-part state sums when T is split into more than one part, plus
+// a final state when the last output is asked for without both M_out and z_out.
+size_t prefill_scratch_bytes(int B, int H, int64_t T, int d, int dv, int segment, la_dtype dtype,
+                             const void* out_last, const float* M_out, const float* z_out);
+
 // Prefill behind la_prefill_state / la_prefill_state_ex (la_api.cu): with use_registered the
 // buffer given to la_set_workspace is the scratch, otherwise (ws, ws_bytes).
 int prefill_impl(const void* q, const void* k, const void* v, void* out_last, const float* M_in, const float* z_in,

@@ -14,22 +14,32 @@ namespace la {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kNoallocMaxDevices = 64;
-static void* g_noalloc_ptr[kNoallocMaxDevices];
+struct NoallocSlot {
+    unsigned long long ctx_id = 0;  // context the address was looked up in
+    void* ptr = nullptr;
+};
+static NoallocSlot g_noalloc[kNoallocMaxDevices];
 static std::mutex g_noalloc_mu;
 
 // Device address of g_noalloc_scratch on the current device. In host code the
 // array's name only stands in for the symbol, so the address must be looked up
-// (once per device, with that device current) before a kernel may be given it.
+// (once per device and context, with that device current) before a kernel may be
+// given it. A new context on the device (after cudaDeviceReset) loads the module
+// anew, so the address is looked up again then.
 static int noalloc_scratch(void** ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) return LA_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != LA_OK) return LA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocSlot& slot = g_noalloc[dev];
+    if (slot.ctx_id != ctx || !slot.ptr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LA_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
+        slot.ptr = p;
+        slot.ctx_id = ctx;
     }
-    *ptr = g_noalloc_ptr[dev];
+    *ptr = slot.ptr;
     return LA_OK;
 }
 
@@ -40,9 +50,12 @@ extern "C" int la_prefill_state_noalloc(const void* q, const void* k, const void
                                         int H, int64_t T, int d, int dv, int segment, float eps, la_dtype dtype,
                                         la_stream_t stream) {
     // argument errors are reported by the prefill itself; only the size limit is checked here
-    const size_t need = la_prefill_workspace_size(B, H, T, d, dv, segment, dtype);
-    if (need > LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_SCRATCH_LIMIT;
     if (!q || !k || !v || B <= 0 || H <= 0 || T <= 0 || segment < 0) return LA_ERR_INVALID_ARG;
+    if (!out_last && !M_out && !z_out) return LA_OK;  // nothing requested
+    for (const float* st : {M_in, z_in, static_cast<const float*>(M_out), static_cast<const float*>(z_out)})
+        if (reinterpret_cast<uintptr_t>(st) & 15u) return LA_ERR_INVALID_ARG;  // as the prefill requires
+    const size_t need = la::prefill_scratch_bytes(B, H, T, d, dv, segment, dtype, out_last, M_out, z_out);
+    if (need > LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_SCRATCH_LIMIT;
     void* ws = nullptr;
     const int rc = la::noalloc_scratch(&ws);
     if (rc != LA_OK) return rc;

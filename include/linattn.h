@@ -110,6 +110,8 @@ size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int 
  * z_T = z_in + sum phi(k_t), out_last = phi(q_T)^T M_T / (phi(q_T)^T z_T + eps).
  *   out_last  [B,H,dv] dtype, written (may be NULL)
  *   M_out, z_out  written (may be NULL); M_out may equal M_in
+ *   M_in, z_in, M_out, z_out  16-byte aligned when given (the parts are summed in
+ *             16-byte vectors); otherwise LA_ERR_INVALID_ARG before any launch
  *   segment   tokens per part (0 = library choice). */
 int la_prefill_state(const void* q, const void* k, const void* v, void* out_last,
                      const float* M_in, const float* z_in, float* M_out, float* z_out,
@@ -139,11 +141,15 @@ size_t la_prefill_workspace_size(int B, int H, int64_t T, int d, int dv, int seg
  * statically sized device variable: every GPU that loads the library holds it until
  * the process exits. The call allocates nothing and runs the same kernels as
  * la_prefill_state_ex with a workspace of that size.
- *   - Returns LA_ERR_SCRATCH_LIMIT, without launching, when
- *     la_prefill_workspace_size(B, H, T, d, dv, segment, dtype) > LA_NOALLOC_SCRATCH_BYTES
- *     (raise `segment` to use fewer parts; every part needs 4*(d*dv + d) bytes per head).
- *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *   - Returns LA_ERR_SCRATCH_LIMIT, without launching, when the scratch this call needs
+ *     is more than LA_NOALLOC_SCRATCH_BYTES. It needs 4*(d*dv + d) bytes per part and
+ *     head when T is split into more than one part (T > segment), plus 4*(d*dv + d) bytes
+ *     per head when out_last is asked for without both M_out and z_out, and nothing
+ *     otherwise. la_prefill_workspace_size counts both terms, so it is an upper bound.
+ *     Raise `segment` to use fewer parts.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current), and so does the first call after a new context was created on the device
+ *     (for example after cudaDeviceReset); make that first call before any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's contents
  *     (every byte a call reads it has written first). Calls whose executions overlap on
  *     the GPU (different streams, not ordered) race on it: order them. */

@@ -26,7 +26,7 @@ Contents
   phi                                  elu(x) + 1
   rel_err_rows / rel_err_state         the tolerance metrics
 
-Readings taken where the pages are silent or garbled (listed in the design doc):
+Readings taken where the pages are silent or garbled:
   phi = elu + 1 on q and k only; eps is added to the denominator; out_t includes
   token t (update then read); the chunk equation's inter term uses the state of
   all tokens before the chunk; no 1/sqrt(d) scaling; state is one (M, z) per head.

@@ -49,6 +49,9 @@ def _load():
         lib.synth_normal.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64,
                                      ctypes.c_double, ctypes.c_int, ctypes.c_void_p]
         lib.synth_normal.restype = None
+        lib.synth_normal_affine.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64,
+                                            ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_void_p]
+        lib.synth_normal_affine.restype = None
         lib.synth_bf16_to_f32.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.synth_bf16_to_f32.restype = None
         _lib = lib
@@ -56,8 +59,9 @@ def _load():
 
 
 def normal(seed: int, tensor_id: int, shape, scale: float = 1.0, dtype: str = "bf16",
-           first: int = 0, out: np.ndarray | None = None) -> np.ndarray:
-    """Values for flat indices [first, first + prod(shape)) of tensor (seed, tensor_id).
+           first: int = 0, out: np.ndarray | None = None, shift: float = 0.0) -> np.ndarray:
+    """shift + scale * N(0,1) for flat indices [first, first + prod(shape)) of tensor
+    (seed, tensor_id).
 
     dtype "bf16" -> uint16 bit patterns, "f32" -> float32. `out` may be a
     preallocated C-contiguous array (e.g. a pinned host buffer viewed as numpy).
@@ -67,9 +71,19 @@ def normal(seed: int, tensor_id: int, shape, scale: float = 1.0, dtype: str = "b
     if out is None:
         out = np.empty(shape, dtype=npdt)
     assert out.dtype == npdt and out.flags.c_contiguous and out.size == n
-    _load().synth_normal(seed, tensor_id, first, n, scale, 1 if dtype == "bf16" else 0,
-                         out.ctypes.data)
+    dt = 1 if dtype == "bf16" else 0
+    if shift == 0.0:
+        _load().synth_normal(seed, tensor_id, first, n, scale, dt, out.ctypes.data)
+    else:
+        _load().synth_normal_affine(seed, tensor_id, first, n, scale, float(shift), dt, out.ctypes.data)
     return out
+
+
+def negate(arr: np.ndarray) -> np.ndarray:
+    """-x of a storage array, exactly (bf16: the sign bit flipped)."""
+    if arr.dtype == np.uint16:
+        return arr ^ np.uint16(0x8000)
+    return -arr
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

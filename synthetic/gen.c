@@ -52,22 +52,30 @@ static inline uint16_t f32_to_bf16_rne(float f) {
     return (uint16_t)(u >> 16);
 }
 
-/* Fill out[0..n) with values for flat indices [first, first + n) of tensor
- * (seed, tensor_id). dtype 0 writes float32, dtype 1 writes bf16 bits. */
-void synth_normal(uint64_t seed, uint64_t tensor_id, uint64_t first, int64_t n,
-                  double scale, int dtype, void* out) {
+/* Fill out[0..n) with shift + scale * N(0,1) for flat indices [first, first + n) of
+ * tensor (seed, tensor_id), computed in float64 and rounded once to float32 (RNE),
+ * then for bf16 storage to bf16 bits. dtype 0 writes float32, dtype 1 bf16 bits. */
+void synth_normal_affine(uint64_t seed, uint64_t tensor_id, uint64_t first, int64_t n,
+                         double scale, double shift, int dtype, void* out) {
     const uint64_t key = stream_key(seed, tensor_id);
     if (dtype == 1) {
         uint16_t* o = (uint16_t*)out;
         #pragma omp parallel for schedule(static)
         for (int64_t j = 0; j < n; ++j)
-            o[j] = f32_to_bf16_rne((float)(scale * normal_at(key, first + (uint64_t)j)));
+            o[j] = f32_to_bf16_rne((float)(shift + scale * normal_at(key, first + (uint64_t)j)));
     } else {
         float* o = (float*)out;
         #pragma omp parallel for schedule(static)
         for (int64_t j = 0; j < n; ++j)
-            o[j] = (float)(scale * normal_at(key, first + (uint64_t)j));
+            o[j] = (float)(shift + scale * normal_at(key, first + (uint64_t)j));
     }
+}
+
+/* The plain recipe: scale * N(0,1) (shift 0 adds an exact zero, so the values are
+ * those of the affine form). */
+void synth_normal(uint64_t seed, uint64_t tensor_id, uint64_t first, int64_t n,
+                  double scale, int dtype, void* out) {
+    synth_normal_affine(seed, tensor_id, first, n, scale, 0.0, dtype, out);
 }
 
 /* Widen bf16 bits to float32 (storage-format conversion only). */
