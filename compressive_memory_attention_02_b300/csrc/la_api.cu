@@ -54,10 +54,14 @@ int current_context_id(unsigned long long* id) {
         get_id = driver_fn<GetId>("cuCtxGetId", 12000);
     });
     if (!get_current || !get_id) return LA_ERR_CUDA;
-    // a runtime call first, so that the device's primary context is current on this thread
-    if (cudaFree(nullptr) != cudaSuccess) return LA_ERR_CUDA;
     CUcontext ctx = nullptr;
-    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS) return LA_ERR_CUDA;
+    if (get_current(&ctx) != CUDA_SUCCESS) return LA_ERR_CUDA;
+    if (!ctx) {
+        // no context on this thread yet: a runtime call makes the device's primary context
+        // current (this cannot happen inside a stream capture, which needs a context)
+        if (cudaFree(nullptr) != cudaSuccess || get_current(&ctx) != CUDA_SUCCESS || !ctx) return LA_ERR_CUDA;
+    }
+    if (get_id(ctx, id) != CUDA_SUCCESS) return LA_ERR_CUDA;
     return LA_OK;
 }
 
@@ -179,7 +183,12 @@ struct FwdPlan {
 static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dtype dtype, int sm_count,
                         bool aliased, size_t ws_avail) {
     FwdPlan pl;
-    const bool tc_shape = (d == 64 || d == 128) && (dv == 64 || dv == 128) && chunk == 64;
+    // The chunk length only sets the blocking: every chunk length gives the same outputs up
+    // to rounding (the chunk equation of mode 3 is the token recurrence regrouped). The
+    // tensor-core kernel works in 64-token chunks whatever length is asked for; the SIMT
+    // kernel uses the length given.
+    (void)chunk;
+    const bool tc_shape = (d == 64 || d == 128) && (dv == 64 || dv == 128);
     pl.tc = dtype == LA_BF16 && tc_shape && env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31);
     if (!pl.tc) return pl;
     const int64_t nch = ceil_div(T, 64);
@@ -205,8 +214,8 @@ static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dt
     }
     if (ws_avail < alias_bytes) return pl;
     // range 0's share of the chunks: range 1 re-forms their state first (measured optimum:
-    // 66% at d = 128, 62% at d = 64, where a chunk's fixed costs weigh more)
-    const int pct = env_int("LA_FWD_SPLIT_PCT", d >= 128 ? 66 : 62);
+    // 70% at d = 128, 64% at d = 64, where a chunk's fixed costs weigh more)
+    const int pct = env_int("LA_FWD_SPLIT_PCT", d >= 128 ? 70 : 64);
     int64_t split = (nch * pct + 50) / 100;
     split = std::max<int64_t>(1, std::min<int64_t>(split, nch - 1));
     pl.nranges = 2;

@@ -7,19 +7,23 @@
 //     den = S'[:, 64] + rowsum(P) + eps                   (= phi(q_t).z_t + eps)
 //     O^T = M_{c-1}^T phi(Q_c)^T + V_c^T P^T              dv x 64 (TMEM)
 //     out = O / den
-//     M^T += V_c^T phi(K_c) (f32 in TMEM),  z += colsum(phi(K_c)) (f32)
+//     M^T += V_c^T phi(K_c) (f32 in TMEM),  z += phi(K_c)^T 1 (f32 in TMEM)
 // M^T is re-cast to bf16 after every update into a second TMEM region, which is the A
 // operand (read from tensor memory) of the next chunk's inter-chunk MMA; the state
-// never passes through shared memory.
+// never passes through shared memory. The key sum z is accumulated on the tensor pipe
+// too: phi(K_c)^T (d x 64) times a constant 64 x 16 tile of ones adds the column sums
+// of phi(K_c) to a 16-column f32 accumulator (every column the same; column 0 is read).
 //
 // One block per (range, head). Warp roles (1024 threads; warp w issues on sub-partition
 // w % 4 and may touch only TMEM lane quarter w % 4):
 //   warp 0        TMA producer: Q, K, V tiles into a 3-stage ring
 //   warp 1        TMEM owner; lane 0 issues every tcgen05.mma, software-pipelined one
 //                 chunk ahead: PV_c, then S'_{c+1}, inter_{c+1}, update_{c+1}
-//   warps 2,3,18-31  F: phi in place on Q and K, zero padded keys, column sums -> z
-//   warps 4-7     R: bf16 re-cast of M^T after each update; final M to global memory
-//   warps 8-15    E: initial state into TMEM; then out = O / den -> bf16 -> swizzled
+//   warps 2,3,18-20,22-24,26-28,30  F: phi in place on Q and K, zero padded keys (none on
+//                 sub-partition 1, which the MMA-issuing warp uses; warps 21, 25, 29, 31 idle)
+//   warps 4-7     R: after each update, z (bf16) into row 64 of the next chunk's K tile and
+//                 the bf16 re-cast of M^T; final M and z to global memory
+//   warps 8-15    E: initial state (M^T and z) into TMEM; then out = O / den -> bf16 -> swizzled
 //                 smem tile (O^T holds one feature per lane: fragments loaded in the
 //                 accumulator layout are stored transposed with stmatrix) -> TMA store;
 //                 warps 8-11 take tokens 0-31, 12-15 tokens 32-63
@@ -36,13 +40,14 @@
 // r at chunk c ^ (r % 8)): Q, K, V tiles as TMA loads them ([64 tokens][64 features]
 // per atom; K atoms have 16 extra rows: row 64 holds bf16 z_{c-1}, rows 65-79 zero);
 // phi(Q), phi(K) read K-major for S' and inter; phi(K), V read MN-major (K = tokens)
-// for the update and PV; P [64 queries][64 keys] K-major.
+// for the update, the key sum and PV; P [64 queries][64 keys] K-major; the ones tile
+// [16][64 tokens] K-major.
 #include "la_tc_common.cuh"
 
 namespace la {
 
 constexpr int FWD_THREADS = 1024;
-constexpr int NFW = 16;  // F warps
+constexpr int NFW = 12;  // F warps
 
 template <int D, int DV>
 struct FwdLayout {
@@ -55,11 +60,10 @@ struct FwdLayout {
     static constexpr int V0 = K0 + NST * KB;
     static constexpr int PT = V0 + NST * VB;     // P, two buffers; an M=128 read past a 64-wide V tile lands here
     static constexpr int OT = PT + 2 * ATOM;     // out tile
-    static constexpr int RDEN = OT + DV / 64 * ATOM;  // 2 x 64 floats
-    static constexpr int ZF = RDEN + 2 * 64 * 4;      // 128 floats
-    static constexpr int ZP = ZF + 128 * 4;           // 2 x NFW x D floats
-    static constexpr int BAR = ZP + 2 * NFW * D * 4;
-    static constexpr int NBAR = 22;
+    static constexpr int ONES = OT + DV / 64 * ATOM;  // 16 x 64 bf16 ones (2 KB, 1024-aligned)
+    static constexpr int RDEN = ONES + 2048;          // 2 x 64 floats
+    static constexpr int BAR = RDEN + 2 * 64 * 4;
+    static constexpr int NBAR = 23;
     static constexpr int MISC = BAR + 8 * NBAR;
     static constexpr int TOTAL = MISC + 16;
     static constexpr int ALLOC = TOTAL + 1024;
@@ -70,6 +74,12 @@ constexpr uint32_t TM_M = 0;     // M^T f32, d columns
 constexpr uint32_t TM_A = 128;   // M^T bf16, two per column: d/2 columns (A operand of inter)
 __device__ __forceinline__ uint32_t tm_s(int buf) { return 192u + 80u * buf; }  // S', 80 columns each
 __device__ __forceinline__ uint32_t tm_o(int buf) { return 352u + 64u * buf; }  // O^T, 64 columns each
+constexpr uint32_t TM_Z = 480;   // z f32, lane = feature, 16 equal columns
+
+// bf16 z_i into row 64 (a multiple of 8: no swizzle offset) of a K tile with atoms ATOMK apart
+__device__ __forceinline__ void put_zrow(uint8_t* ktile, int i, float z) {
+    *reinterpret_cast<__nv_bfloat16*>(ktile + (i >> 6) * ATOMK + 64 * 128 + (i & 63) * 2) = __float2bfloat16_rn(z);
+}
 
 // 16 f32 values -> 8 words of two bf16 (low half = even index)
 __device__ __forceinline__ void pack16_bf16(const uint32_t* x, uint32_t* a) {
@@ -86,8 +96,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     float* rden = reinterpret_cast<float*>(sm + L::RDEN);
-    float* zf = reinterpret_cast<float*>(sm + L::ZF);
-    float* zpart = reinterpret_cast<float*>(sm + L::ZP);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     uint64_t* full = bars + 0;      // [3] TMA landed
     uint64_t* empty = bars + 3;     // [3] stage free (MMA commit)
@@ -100,6 +108,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     uint64_t* upd_done = bars + 19; // state update finished (MMA commit)
     uint64_t* mt_ready = bars + 20; // bf16 M^T written and TMEM M read (R)
     uint64_t* drain = bars + 21;    // all MMAs finished (MMA thread only)
+    uint64_t* zrow_ready = bars + 22; // z before the next main chunk in its K tile's row 64 (E, then R)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -134,6 +143,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     if (warp == 1) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
+    }
+    if (warp >= 2 && warp < 6) {  // the ones tile of the key-sum MMA: 2048 bytes of bf16 1.0
+        const uint32_t one2 = 0x3F803F80u;
+        reinterpret_cast<uint4*>(sm + L::ONES)[threadIdx.x - 64] = make_uint4(one2, one2, one2, one2);
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -179,6 +193,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             constexpr uint32_t id_u = idesc_bf16(128, D, 1, 1);      // M^T += V^T phiK
             constexpr uint32_t id_pv = idesc_bf16(128, CH, 1, 0);    // O^T += V^T P^T
             constexpr uint32_t id_in = idesc_bf16(128, CH, 0, 0);    // O^T = M^T phiQ^T
+            constexpr uint32_t id_z = idesc_bf16(128, 16, 1, 0);     // z (x16) += phiK^T 1
             // Descriptors of stage 0 / buffer 0; others differ only in the start-address field
             // (bits 0-13, address >> 4), which stays below 2^14 for any shared-memory address,
             // so an offset is added to the descriptor directly.
@@ -187,6 +202,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             const uint64_t dku0 = sdesc_sw128(smem_u32(sm + L::K0), ATOMK, 1024); // phiK, MN-major
             const uint64_t dv0 = sdesc_sw128(smem_u32(sm + L::V0), ATOM, 1024);   // V, MN-major
             const uint64_t dp0 = sdesc_sw128(smem_u32(sm + L::PT), 16, 1024);     // P, K-major
+            const uint64_t d1 = sdesc_sw128(smem_u32(sm + L::ONES), 16, 1024);    // ones, K-major
             auto off = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
             bool ok = true;
             int mt_waits = 0;
@@ -202,6 +218,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks)
                     mma_bf16_ss(tmem + TM_M, va + off(ks * 2048), kb + off(ks * 2048), id_u, 1);
+#pragma unroll
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    mma_bf16_ss(tmem + TM_Z, kb + off(ks * 2048), d1 + off(ks * 32), id_z, 1);
             };
             // S'_m, inter_m, update_m of main chunk m
             auto front = [&](int m) {
@@ -209,6 +228,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 const uint64_t qd = dq0 + off(s * L::QB), kd = dk0 + off(s * L::KB);
                 if (!wait(&phib[s], (g / NST) & 1)) return false;
                 if (m >= 2 && !wait(&s_free[buf], ((m >> 1) - 1) & 1)) return false;
+                if (!wait(zrow_ready, m & 1)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -255,12 +275,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             mbar_wait_drain(drain, 0);
         }
     } else if (warp >= 4 && warp < 8) {
-        // ======================================================== R: state re-cast
+        // ======================================================== R: z row and state re-cast
         const int ct = threadIdx.x - 128;
         const int q = warp & 3;
-        const int j = 32 * q + lane;              // dv row of M^T
+        const int j = 32 * q + lane;              // dv row of M^T; feature of z
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const bool has_row = 32 * q < DV;         // warp-uniform
+        const bool has_z = 32 * q < D;            // warp-uniform
         auto recast = [&]() {
             if (!has_row) return;
 #pragma unroll 1
@@ -281,19 +302,36 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             if (u + 1 < n_upd) {
+                // the main chunk after this update: its S' reads z from row 64 of its K tile
+                const int mnext = n_agg > 0 ? u : u + 1;
+                if (has_z) {
+                    const uint32_t zb = tmem_ld1(tmem + TM_Z + lane_base);
+                    tmem_wait_ld();
+                    put_zrow(sm + L::K0 + ((n_agg + mnext) % NST) * L::KB, j, __uint_as_float(zb));
+                    fence_proxy_async_smem();
+                }
+                named_bar_sync(4, 128);
+                if (ct == 0) mbar_arrive(zrow_ready);
                 recast();
                 tc_fence_before();
                 named_bar_sync(4, 128);
                 if (ct == 0) mbar_arrive(mt_ready);
-            } else if (writes_state && p.M_out && has_row) {
-                float* dst = p.M_out + (int64_t)bh * D * DV + j;
-#pragma unroll 1
-                for (int i0 = 0; i0 < D; i0 += 16) {
-                    uint32_t x[16];
-                    tmem_ld16(tmem + TM_M + lane_base + i0, x);
+            } else if (writes_state) {
+                if (p.z_out && has_z) {
+                    const uint32_t zb = tmem_ld1(tmem + TM_Z + lane_base);
                     tmem_wait_ld();
+                    p.z_out[(int64_t)bh * D + j] = __uint_as_float(zb);
+                }
+                if (p.M_out && has_row) {
+                    float* dst = p.M_out + (int64_t)bh * D * DV + j;
+#pragma unroll 1
+                    for (int i0 = 0; i0 < D; i0 += 16) {
+                        uint32_t x[16];
+                        tmem_ld16(tmem + TM_M + lane_base + i0, x);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) dst[(int64_t)(i0 + e) * DV] = __uint_as_float(x[e]);
+                        for (int e = 0; e < 16; ++e) dst[(int64_t)(i0 + e) * DV] = __uint_as_float(x[e]);
+                    }
                 }
             }
         }
@@ -331,9 +369,24 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             }
             tmem_wait_st();
         }
+        if (hf == 0 && 32 * q < D) {
+            // z_in (+ range aggregates) into TMEM; with no state-only chunks before the first
+            // main chunk it is also z before that chunk (row 64 of its K tile, stage 0)
+            float zz = p.z_in ? p.z_in[(int64_t)bh * D + j] : 0.f;
+            for (int pp = 0; pp < nws; ++pp) zz += agg[pp * p.rec + D * DV + j];
+            tmem_st1(tmem + TM_Z + lane_base, __float_as_uint(zz));
+            tmem_wait_st();
+            if (n_agg == 0) {
+                put_zrow(sm + L::K0, j, zz);
+                fence_proxy_async_smem();
+            }
+        }
         tc_fence_before();
         named_bar_sync(3, 256);
-        if (ct == 0) mbar_arrive(mt_ready);
+        if (ct == 0) {
+            mbar_arrive(mt_ready);
+            if (n_agg == 0) mbar_arrive(zrow_ready);
+        }
 
         // Thread l of the warp stores, per stmatrix, row (l % 8) of matrix l / 8: features
         // f0 .. f0+7 (f0 = 32q + 8(l / 8)) of token 32hf + 8i + (l % 8), i = 0..3; the row's
@@ -402,7 +455,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             uint8_t* prow = sm + L::PT + buf * ATOM + t * 128;
-            uint64_t rowsum2 = 0;  // (even keys, odd keys) partial sums
+            uint64_t rowsum2 = 0;  // (even keys, odd keys) partial sums of the f32 scores
             const uint32_t srow = tmem + tm_s(buf) + lane_base;
             // keys 32h .. 32h+31 of the row from x[0..32): P as bf16 into the swizzled tile, row sum
             auto half = [&](const uint32_t* x, int h, bool diag) {
@@ -419,7 +472,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                             s1 = (c0 + 1 <= t) ? s1 : 0.f;
                         }
                         pk[jj] = pack_bf16(s0, s1);
-                        rowsum2 = f2_add(rowsum2, f2_pack(bf16lo(pk[jj]), bf16hi(pk[jj])));
+                        rowsum2 = f2_add(rowsum2, f2_pack(s0, s1));
                     }
                     *reinterpret_cast<uint4*>(prow + (((4 * h + g8) ^ (t & 7)) << 4)) =
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -436,14 +489,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 for (int g8 = 4; g8 < 8; ++g8)
                     *reinterpret_cast<uint4*>(prow + ((g8 ^ (t & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
             } else {       // rows 32-63: keys 0-31 all lie before the row
-                uint32_t x[32];
+                uint32_t x[32], y[32];
                 tmem_ld32(srow, x);
-                tmem_wait_ld();
-                half(x, 0, false);
-                tmem_ld32(srow + 32, x);
+                tmem_ld32(srow + 32, y);
                 zq = tmem_ld1(srow + 64);
                 tmem_wait_ld();
-                half(x, 1, true);
+                half(x, 0, false);
+                half(y, 1, true);
             }
             rden[buf * 64 + t] = 1.f / (__uint_as_float(zq) + (f2_lo(rowsum2) + f2_hi(rowsum2)) + p.eps);
             tc_fence_before();
@@ -455,64 +507,29 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             }
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
-    } else {
-        // ======================================================== F: phi and z (warps 2, 3, 18-31)
-        const int ct = (warp < 4 ? warp - 2 : warp - 16) * 32 + lane;
-        if (ct < D) {
-            float zz = p.z_in ? p.z_in[(int64_t)bh * D + ct] : 0.f;
-            for (int pp = 0; pp < nws; ++pp) zz += agg[pp * p.rec + D * DV + ct];
-            zf[ct] = zz;
-        }
+    } else if (warp != 21 && warp != 25 && warp != 29 && warp != 31) {
+        // ======================================================== F: phi (warps 2, 3, 18-30 but 21, 25, 29)
+        const int fi = warp < 4 ? warp - 2 : 2 + (warp - 18) - (warp - 17) / 4;
+        const int ct = fi * 32 + lane;
         for (int idx = ct; idx < NST * (D / 64) * 15 * 8; idx += 32 * NFW) {
             const int c16 = idx % 8, row = 65 + (idx / 8) % 15, sa = idx / (8 * 15);
             *reinterpret_cast<uint4*>(sm + L::K0 + sa * ATOMK + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
         }
-        named_bar_sync(1, 32 * NFW);
         bool ok = true;
-        float colsum_agg[8];  // state-only chunks: column sums kept in registers, folded once at the end
-#pragma unroll
-        for (int e = 0; e < 8; ++e) colsum_agg[e] = 0.f;
         for (int g = 0; g < nchunks; ++g) {
             const int s = g % NST;
             const bool is_main = g >= n_agg;
             ok = bar_and(1, 32 * NFW, mbar_wait(&full[s], (g / NST) & 1, abort_flag));
             if (!ok) break;
-            uint8_t* qb = sm + L::Q0 + s * L::QB;
-            uint8_t* kb = sm + L::K0 + s * L::KB;
             const int64_t t0 = (int64_t)(is_main ? main_begin + g - n_agg : g) * CH;
             const int valid = (int)min64(CH, p.T - t0);
-            if (is_main && ct < D)  // row 64 (a multiple of 8: no swizzle offset) carries z before this chunk
-                *reinterpret_cast<__nv_bfloat16*>(kb + (ct >> 6) * ATOMK + 64 * 128 + (ct & 63) * 2) =
-                    __float2bfloat16_rn(zf[ct]);
-            if (!is_main) {
-                // z is needed only after the last state-only chunk: no per-chunk reduction
-                phi_tile<D, 32 * NFW>(kb, ATOMK, valid, ct, colsum_agg);
-                fence_proxy_async_smem();
-                named_bar_sync(1, 32 * NFW);
-                if (ct == 0) mbar_arrive(&phib[s]);
-                if (g + 1 < n_agg) continue;
-            }
-            float colsum[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) colsum[e] = is_main ? 0.f : colsum_agg[e];
-            if (is_main) {
-                phi_tile<D, 32 * NFW>(qb, ATOM, CH, ct, nullptr);
-                phi_tile<D, 32 * NFW>(kb, ATOMK, valid, ct, colsum);
-            }
-            float* zp = zpart + (g & 1) * NFW * D;
-            colsum_to_smem<D>(colsum, zp, ct);
-            if (is_main) fence_proxy_async_smem();
+            if (is_main) phi_tile<D, 32 * NFW>(sm + L::Q0 + s * L::QB, ATOM, CH, ct, nullptr);
+            phi_tile<D, 32 * NFW>(sm + L::K0 + s * L::KB, ATOMK, valid, ct, nullptr);
+            fence_proxy_async_smem();
             named_bar_sync(1, 32 * NFW);
-            if (ct == 0 && is_main) mbar_arrive(&phib[s]);
-            if (ct < D) {
-                float zz = zf[ct];
-#pragma unroll
-                for (int w = 0; w < NFW; ++w) zz += zp[w * D + ct];
-                zf[ct] = zz;
-            }
+            if (ct == 0) mbar_arrive(&phib[s]);
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
-        if (ok && writes_state && p.z_out && ct < D) p.z_out[(int64_t)bh * D + ct] = zf[ct];
     }
 
     tc_fence_before();

@@ -65,19 +65,18 @@ __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
 }
 
 // phi in place on a [64 x D] bf16 tile (atoms `astride` bytes apart), by NT threads.
-// Thread ct owns 16-byte chunk column j = ct % (D/8) of rows g, g + RG, ...
+// Thread ct owns 16-byte chunk column j = ct % (D/8) of rows g, g + RG, ... below 64
 // (g = ct / (D/8)); since RG is a multiple of 8 the swizzled chunk position
 // j ^ (row % 8) is the same for all of its rows. Rows >= valid become 0 (phi(0) = 1
 // must not enter the sums; pass valid = 64 to keep all rows). With colsum != nullptr
 // the thread adds the bf16-rounded results of its 8 columns into colsum[0..8).
-// Kept as a compact loop: this code runs beside other warp roles on the same
-// sub-partitions and must stay resident in the instruction caches.
+// The row loop is unrolled so that a thread's rows are in flight together.
 template <int D, int NT = 128>
 __device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, int ct, float* colsum) {
     constexpr int CPR = D / 8;
     constexpr int RG = NT / CPR;
-    static_assert(RG % 8 == 0 && CH % RG == 0, "rows of a thread share one swizzle phase");
-    constexpr int RPT = CH / RG;
+    static_assert(RG % 8 == 0, "rows of a thread share one swizzle phase");
+    constexpr int RPT = (CH + RG - 1) / RG;
     const int j = ct % CPR, g = ct / CPR;
     uint4* base = reinterpret_cast<uint4*>(tile + (j >> 3) * astride + (((j & 7) ^ (g & 7)) << 4) + g * 128);
     uint64_t cs[4];  // column sums as f32 pairs
@@ -85,8 +84,9 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, 
 #pragma unroll
         for (int e = 0; e < 4; ++e) cs[e] = f2_pack(colsum[2 * e], colsum[2 * e + 1]);
     }
-#pragma unroll 1
+#pragma unroll
     for (int i = 0; i < RPT; ++i) {
+        if (CH % RG != 0 && g + i * RG >= CH) break;
         uint4 x = base[i * RG * 8];
         uint32_t w[4] = {x.x, x.y, x.z, x.w};
         if (g + i * RG < valid) {

@@ -37,8 +37,11 @@
  * Supported: dtype LA_F32 or LA_BF16 for q/k/v/out (same type for all four;
  * state is always float32); 1 <= d, dv <= 128 with d, dv multiples of 8;
  * T >= 1; chunk in {16, 32, 64, 128}. The bf16 tensor-core path takes
- * d, dv in {64, 128}, chunk 64, 16-byte aligned pointers and strides that are
- * multiples of 8 elements; other bf16 shapes run on the SIMT path.
+ * d, dv in {64, 128}, 16-byte aligned pointers and strides that are multiples of
+ * 8 elements; other bf16 shapes run on the SIMT path. `chunk` sets the blocking
+ * only (every chunk length gives the same outputs up to rounding): the
+ * tensor-core path always works in 64-token chunks, the SIMT path (float32, and
+ * bf16 shapes outside the tensor-core set) in chunks of the given length.
  */
 #ifndef LINATTN_H
 #define LINATTN_H

@@ -1,7 +1,9 @@
-"""The N > 1 path of the benchmark, on CPU: two gloo ranks each run their own replica
-of a (small) segmented workload through the float64 oracle, with the seed, input
-layout and max-over-ranks timing reduction that bench.py uses on GPUs (weak scaling,
-no data-path collective)."""
+"""The N > 1 path: on CPU, two gloo ranks each run their own replica of a (small)
+segmented workload through the float64 oracle, with the seed, input layout and
+max-over-ranks timing reduction that bench.py uses on GPUs (weak scaling, no data-path
+collective); on a GPU, two ranks each call the library on their shard of the heads
+(the head split needs no exchange) and rank 0 checks the gathered result against one
+call over all heads."""
 import dataclasses
 import multiprocessing as mp
 import os
@@ -9,6 +11,7 @@ import socket
 import sys
 
 import numpy as np
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -86,3 +89,97 @@ def test_single_rank_reduction_is_identity():
     import bench
     assert bench.max_over_ranks(3.25, None, "cpu") == 3.25
     assert bench.aggregate_rate(1000, 2.0, 1) == 500.0
+
+
+# ---------------------------------------------------------------------------- the library on two ranks
+
+def _gpu_worker(rank, world, port, queue, ranges):
+    """Rank `rank` runs la_causal_fwd_ex on its shard of the (b, h) heads of one problem:
+    heads [rank*H/2, (rank+1)*H/2) of every batch, read and written in place through the
+    strided call (element strides of the full [B, H, T, d] tensors), with its own state."""
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    if ranges:
+        os.environ["LA_FWD_RANGES"] = str(ranges)
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import compressive_memory_attention_02_b300 as la
+        from gpu_helpers import to_dev
+        import synthetic
+        torch.cuda.set_device(0)
+        B, H, T, d = 2, 8, 1000, 128
+        q = to_dev(synthetic.normal(81, 0, (B, H, T, d), 0.5, "bf16"))
+        k = to_dev(synthetic.normal(81, 1, (B, H, T, d), 0.5, "bf16"))
+        v = to_dev(synthetic.normal(81, 2, (B, H, T, d), 0.5, "bf16"))
+        Hs = H // world
+        h0 = rank * Hs
+        out = torch.zeros(B, H, T, d, dtype=torch.bfloat16, device="cuda")
+        M = torch.empty(B, Hs, d, d, device="cuda")
+        z = torch.empty(B, Hs, d, device="cuda")
+        st = [H * T * d, T * d, d] * 4
+        sl = lambda t: t[:, h0:h0 + Hs]
+        nws = la.la_causal_fwd_workspace_size(B, Hs, T, d, d, 64, la.LA_BF16)
+        ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+        la.la_causal_fwd_ex(sl(q), sl(k), sl(v), sl(out), None, None, M, z, B, Hs, T, d, d, 64, 1e-6, la.LA_BF16,
+                            st, ws, nws)
+        torch.cuda.synchronize()
+        assert la.la_get_last_device_status() == la.LA_OK
+        # gather the shards on rank 0 (gloo, host tensors): the head-sharded job's result
+        parts = [torch.empty(B, Hs, T, d, dtype=torch.bfloat16) for _ in range(world)]
+        Ms = [torch.empty(B, Hs, d, d) for _ in range(world)]
+        dist.all_gather(parts, sl(out).cpu().contiguous())
+        dist.all_gather(Ms, M.cpu())
+        if rank == 0:
+            full_o = torch.cat(parts, dim=1)
+            full_M = torch.cat(Ms, dim=1)
+            # the single-process call over all heads
+            o1 = torch.empty(B, H, T, d, dtype=torch.bfloat16, device="cuda")
+            M1 = torch.empty(B, H, d, d, device="cuda")
+            z1 = torch.empty(B, H, d, device="cuda")
+            nws = la.la_causal_fwd_workspace_size(B, H, T, d, d, 64, la.LA_BF16)
+            ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+            la.la_causal_fwd_ex(q, k, v, o1, None, None, M1, z1, B, H, T, d, d, 64, 1e-6, la.LA_BF16, None, ws, nws)
+            torch.cuda.synchronize()
+            o1, M1 = o1.cpu(), M1.cpu()
+            exact = bool(torch.equal(full_o, o1) and torch.equal(full_M, M1))
+            diff = float((full_o.float() - o1.float()).abs().max() / o1.float().abs().max())
+            queue.put(("ok", exact, diff))
+        dist.barrier()
+    except Exception as e:  # report instead of hanging the other rank's queue read
+        queue.put(("error", repr(e), 0.0))
+        raise
+    finally:
+        dist.destroy_process_group()
+
+
+def _run_two_gpu_ranks(ranges):
+    ctx = mp.get_context("spawn")
+    queue = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gpu_worker, args=(r, 2, port, queue, ranges)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = queue.get(timeout=300)
+    for p in procs:
+        p.join(timeout=120)
+    assert res[0] == "ok", res
+    assert all(p.exitcode == 0 for p in procs)
+    return res
+
+
+@pytest.mark.gpu
+def test_head_sharded_library_calls_on_two_ranks_equal_one_call_bit_for_bit():
+    # a fixed number of ranges per head: each head is computed the same way in both jobs
+    _, exact, diff = _run_two_gpu_ranks(ranges=2)
+    assert exact, diff
+
+
+@pytest.mark.gpu
+def test_head_sharded_library_calls_with_default_schedules_match_within_tolerance():
+    # the default schedule depends on the number of heads per call, so rounding may differ
+    _, exact, diff = _run_two_gpu_ranks(ranges=0)
+    assert diff <= 2e-2

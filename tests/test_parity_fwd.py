@@ -197,3 +197,54 @@ def test_segmented_workload_full_sampled_heads():
     # properties over every head: outputs inside the hull of the values seen so far
     vmax = torch.cummax(tv.float().abs(), dim=2).values
     assert bool((out.float().abs() <= vmax * 1.02 + 1e-6).all())
+
+
+def test_bf16_calls_captured_in_a_cuda_graph_match_eager_calls():
+    """Segment calls chained through M, z, captured in one CUDA graph and replayed, give the
+    eager calls' results bit for bit (the calls make no synchronising CUDA call)."""
+    import compressive_memory_attention_02_b300 as la
+    B, H, S, Tseg, d = 2, 4, 3, 256, 128
+    q, k, v = _inputs(50, B, H, S * Tseg, d, d, "bf16", 0.5)
+    seg = lambda a, s: to_dev(np.ascontiguousarray(a[:, :, s * Tseg:(s + 1) * Tseg]))
+    qs, ks, vs = [seg(q, s) for s in range(S)], [seg(k, s) for s in range(S)], [seg(v, s) for s in range(S)]
+    nws = la.la_causal_fwd_workspace_size(B, H, Tseg, d, d, 64, la.LA_BF16)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+
+    def run(outs, Ms, zs):
+        for s in range(S):
+            Mi, zi = (None, None) if s == 0 else (Ms[s - 1], zs[s - 1])
+            la.la_causal_fwd_ex(qs[s], ks[s], vs[s], outs[s], Mi, zi, Ms[s], zs[s], B, H, Tseg, d, d, 64, 1e-6,
+                                la.LA_BF16, None, ws, nws)
+
+    mk = lambda: ([torch.empty(B, H, Tseg, d, dtype=torch.bfloat16, device="cuda") for _ in range(S)],
+                  [torch.empty(B, H, d, d, device="cuda") for _ in range(S)],
+                  [torch.empty(B, H, d, device="cuda") for _ in range(S)])
+    eager = mk()
+    run(*eager)
+    torch.cuda.synchronize()
+    graphed = mk()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run(*graphed)
+    g.replay()
+    torch.cuda.synchronize()
+    assert la.la_get_last_device_status() == la.LA_OK
+    for a, b in zip(eager, graphed):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 128])
+def test_bf16_any_chunk_length_runs_on_the_tensor_core_path(chunk):
+    """The chunk length is a blocking choice: the bf16 tensor-core shapes run the same
+    64-token tensor-core kernel for every chunk length (identical results), and match the
+    oracle."""
+    import compressive_memory_attention_02_b300 as la
+    q, k, v = _inputs(51, 1, 3, 700, 128, 128, "bf16", 0.5)
+    tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
+    a = fwd(tq, tk, tv, chunk=chunk)
+    b = fwd(tq, tk, tv, chunk=64)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    _compare(a, oracle.causal_fwd(q, k, v), TOL_BF16)
