@@ -13,11 +13,13 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "liblinattn.so")
+# LA_CHECKED=1 loads the checked library (device-side bounds checks, see la_checked_build)
+LIB_PATH = os.path.join(_HERE, "liblinattn_checked.so" if os.environ.get("LA_CHECKED") == "1" else "liblinattn.so")
 
 LA_F32, LA_BF16 = 0, 1
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_ERR_SCRATCH_LIMIT = 6
+LA_ERR_BOUNDS = 7
 LA_NOALLOC_SCRATCH_BYTES = 32 << 20  # size of the library's static prefill scratch
 
 EXPORTS = (
@@ -25,7 +27,8 @@ EXPORTS = (
     "la_prefill_state", "la_prefill_state_ex", "la_prefill_workspace_size", "la_prefill_state_noalloc",
     "la_decode_step", "la_causal_bwd", "la_causal_bwd_ex", "la_causal_bwd_workspace_size",
     "la_set_workspace", "la_get_last_device_status",
-    "la_get_error_string", "la_last_launch_count", "la_selftest_wait_timeout",
+    "la_get_error_string", "la_last_launch_count", "la_selftest_wait_timeout", "la_checked_build",
+    "la_feature_map_prf", "la_causal_fwd_mapped",
 )
 
 
@@ -45,6 +48,8 @@ def _load() -> ctypes.CDLL:
     fwd = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, f32, i32]
     lib.la_causal_fwd.argtypes = fwd + [vp]
     lib.la_causal_fwd_ex.argtypes = fwd + [i64p, vp, sz, vp]
+    lib.la_causal_fwd_mapped.argtypes = fwd + [i64p, vp, sz, vp]
+    lib.la_feature_map_prf.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp]
     lib.la_causal_fwd_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32]
     lib.la_causal_fwd_workspace_size.restype = sz
     lib.la_prefill_state.argtypes = fwd + [vp]
@@ -63,6 +68,7 @@ def _load() -> ctypes.CDLL:
     lib.la_get_error_string.argtypes = [i32]
     lib.la_get_error_string.restype = ctypes.c_char_p
     lib.la_last_launch_count.argtypes = []
+    lib.la_checked_build.argtypes = []
     lib.la_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
     for name in EXPORTS:
         f = getattr(lib, name)
@@ -134,6 +140,19 @@ def la_causal_fwd_ex(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chu
                               _ptr(z_out), B, H, T, d, dv, chunk, eps, _dtype(dtype, q), _strides(strides),
                               _ptr(workspace), int(workspace_bytes), _stream(stream, q))
     return _check("la_causal_fwd_ex", rc)
+
+
+def la_causal_fwd_mapped(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chunk, eps,
+                         dtype=None, strides=None, workspace=None, workspace_bytes=0, stream=None):
+    rc = lib.la_causal_fwd_mapped(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(M_in), _ptr(z_in), _ptr(M_out),
+                                  _ptr(z_out), B, H, T, d, dv, chunk, eps, _dtype(dtype, q), _strides(strides),
+                                  _ptr(workspace), int(workspace_bytes), _stream(stream, q))
+    return _check("la_causal_fwd_mapped", rc)
+
+
+def la_feature_map_prf(x, W, out, rows, d, m, dtype=None, stream=None):
+    rc = lib.la_feature_map_prf(_ptr(x), _ptr(W), _ptr(out), rows, d, m, _dtype(dtype, x), _stream(stream, x))
+    return _check("la_feature_map_prf", rc)
 
 
 def la_causal_fwd_workspace_size(B, H, T, d, dv, chunk, dtype) -> int:
@@ -215,6 +234,10 @@ def la_selftest_wait_timeout(limit_cycles, stream=None):
 
 def la_last_launch_count() -> int:
     return int(lib.la_last_launch_count())
+
+
+def la_checked_build() -> int:
+    return int(lib.la_checked_build())
 
 
 _workspaces = {}

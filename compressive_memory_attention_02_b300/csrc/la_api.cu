@@ -163,6 +163,32 @@ static bool strides_tma(const Strides& s, bool with_out) {
 
 static int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 
+// Elements spanned by a strided [B, H, T, inner] tensor.
+static int64_t span(int B, int H, int64_t T, int inner, int64_t sb, int64_t sh, int64_t st) {
+    return (int64_t)(B - 1) * sb + (int64_t)(H - 1) * sh + (T - 1) * st + inner;
+}
+
+// Extents of the caller's buffers for the checked build's device-side bounds checks. In
+// that build only, LA_CHECKS_SHRINK=n declares every extent n elements shorter than the
+// buffer really is: accesses to the last n elements are then reported (LA_ERR_BOUNDS) and
+// skipped, while every access made stays inside the real buffer. It exists to test the
+// reporting path without touching memory outside an allocation.
+static Extents make_extents(int B, int H, int64_t T, int d, int dv, const Strides& st, int64_t ws_floats) {
+    Extents e;
+    e.q = span(B, H, T, d, st.q_sb, st.q_sh, st.q_st);
+    e.k = span(B, H, T, d, st.k_sb, st.k_sh, st.k_st);
+    e.v = span(B, H, T, dv, st.v_sb, st.v_sh, st.v_st);
+    e.o = span(B, H, T, dv, st.o_sb, st.o_sh, st.o_st);
+    e.M_in = e.M_out = (int64_t)B * H * d * dv;
+    e.z_in = e.z_out = (int64_t)B * H * d;
+    e.ws = ws_floats;
+#if LA_CHECKS
+    const int64_t shrink = env_int("LA_CHECKS_SHRINK", 0);
+    for (int64_t* x : {&e.q, &e.k, &e.v, &e.o, &e.M_in, &e.z_in, &e.M_out, &e.z_out, &e.ws}) *x -= shrink;
+#endif
+    return e;
+}
+
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------------ forward
@@ -227,7 +253,7 @@ static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dt
 static int fwd_impl(const void* q, const void* k, const void* v, void* out, const float* M_in, const float* z_in,
                     float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv, int chunk, float eps,
                     la_dtype dtype, const int64_t* strides, void* ws, size_t ws_bytes, bool use_registered,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, bool phi_ident = false) {
     t_launches = 0;
     if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || T <= 0 || !(eps >= 0.f)) return LA_ERR_INVALID_ARG;
@@ -284,12 +310,13 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
             pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv;
             pp.part_len = (int64_t)pl.chunks_per_range * 64;
             pp.nparts = pl.nranges - 1;
-            pp.eps = eps, pp.st = st, pp.status = ds->status;
+            pp.eps = eps, pp.st = st, pp.status = ds->status, pp.phi_ident = phi_ident;
             rc = cuda_rc(launch_parts_tc(pp, mk, mv, stream));
             if (rc) return rc;
             ++t_launches;
         }
         FwdTcParams fp{};
+        fp.phi_ident = phi_ident;
         fp.M_in = Mi, fp.z_in = zi, fp.M_out = M_out, fp.z_out = z_out;
         fp.ws = pl.nranges > 2 ? wsf : nullptr;
         fp.rec = rec, fp.nranges = pl.nranges, fp.chunks_per_range = pl.chunks_per_range, fp.split = pl.split;
@@ -302,6 +329,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
     FwdParams p{};
     p.q = q, p.k = k, p.v = v, p.out = out, p.M_in = M_in, p.z_in = z_in, p.M_out = M_out, p.z_out = z_out;
     p.B = B, p.H = H, p.T = T, p.d = d, p.dv = dv, p.chunk = chunk, p.eps = eps, p.st = st;
+    p.ext = make_extents(B, H, T, d, dv, st, 0), p.status = ds->status, p.phi_ident = phi_ident;
     rc = cuda_rc(launch_fwd_simt(p, dtype == LA_BF16, stream));
     if (!rc) ++t_launches;
     return rc;
@@ -385,6 +413,13 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
         if (!fz) fz = fin + BH * d * dv;
     }
     const bool bf16 = dtype == LA_BF16;
+    // extents for the checked build: out_last is [B, H, dv]; the part records (when T is
+    // split) are BH * nparts records of rec floats from wsf
+    Extents ext = make_extents(B, H, T, d, dv, st, pl.nparts > 1 ? BH * pl.nparts * rec : 0);
+    ext.o = BH * dv;
+#if LA_CHECKS
+    ext.o -= env_int("LA_CHECKS_SHRINK", 0);
+#endif
 
     if (need_final && (!fM || !fz)) {
         // no place for a final state: the SIMT kernel keeps it on chip and reads out itself
@@ -394,6 +429,7 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
         pp.dst_M = M_out, pp.dst_z = z_out, pp.rec_M = (int64_t)d * dv, pp.rec_z = d;
         pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv, pp.part_len = T, pp.nparts = 1;
         pp.eps = eps, pp.st = st, pp.status = ds->status;
+        pp.ext = ext;
         rc = cuda_rc(launch_parts_simt(pp, bf16, stream));
         if (!rc) ++t_launches;
         return rc;
@@ -408,11 +444,13 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
     pp.q = q, pp.k = k, pp.v = v;
     pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv, pp.part_len = pl.part_len, pp.nparts = pl.nparts;
     pp.eps = eps, pp.st = st, pp.status = ds->status;
+    pp.ext = ext;
     if (pl.nparts == 1) {
         pp.base_M = M_in, pp.base_z = z_in;
         pp.dst_M = fM, pp.dst_z = fz, pp.rec_M = (int64_t)d * dv, pp.rec_z = d;
     } else {
         pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv, pp.rec_M = rec, pp.rec_z = rec;
+        pp.ext.M_out = ext.ws, pp.ext.z_out = ext.ws - (int64_t)d * dv;  // the record array
     }
     if (pl.tc) {
         if (!pp.dst_M || !pp.dst_z) {
@@ -440,6 +478,7 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
         rp.base_M = M_in, rp.base_z = z_in, rp.parts_M = wsf, rp.parts_z = wsf + (size_t)d * dv;
         rp.rec_M = rec, rp.rec_z = rec, rp.dst_M = fM, rp.dst_z = fz;
         rp.BH = (int)BH, rp.d = d, rp.dv = dv, rp.nparts = pl.nparts;
+        rp.ext = ext, rp.status = ds->status;
         if (!fM || !fz) return LA_ERR_INVALID_ARG;  // unreachable: both set when parts > 1
         rc = cuda_rc(launch_reduce_parts(rp, stream));
         if (rc) return rc;
@@ -448,7 +487,7 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out_last, co
     if (out_last) {
         PrefillOutParams op{};
         op.q = q, op.out = out_last, op.M = fM, op.z = fz, op.B = B, op.H = H, op.T = T, op.d = d, op.dv = dv;
-        op.eps = eps, op.st = st;
+        op.eps = eps, op.st = st, op.ext = ext, op.status = ds->status;
         rc = cuda_rc(launch_prefill_out(op, bf16, stream));
         if (rc) return rc;
         ++t_launches;
@@ -489,6 +528,48 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
     float* wsf = static_cast<float*>(ws);
     const int64_t rec = (int64_t)d * dv_dim + d;
     const bool bf16 = dtype == LA_BF16;
+
+    const bool tc = bf16 && (d == 64 || d == 128) && (dv_dim == 64 || dv_dim == 128) &&
+                    env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31);
+    if (tc) {
+        // tensor-core chunk kernels: per-chunk key-value sums (parts_tc with 64-token parts),
+        // the prefix scan, dq (with g, e and the chunk sums of the state gradient), the
+        // reverse scan, then dk and dv
+        const Strides st = contiguous(H, T, d, dv_dim);
+        CUtensorMap mq, mk, mv, mdo, mg;
+        void* G = wsf + off_G;
+        if (!make_map(&mq, q, d, T, H, B, st.q_st, st.q_sh, st.q_sb) ||
+            !make_map(&mk, k, d, T, H, B, st.k_st, st.k_sh, st.k_sb) ||
+            !make_map(&mv, v, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
+            !make_map(&mdo, dout, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
+            !make_map(&mg, G, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb))
+            return LA_ERR_CUDA;
+        PartsParams pp{};
+        pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv_dim, pp.rec_M = rec, pp.rec_z = rec;
+        pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv_dim, pp.part_len = BWD_CH, pp.nparts = (int)nch;
+        pp.eps = eps, pp.st = st, pp.status = ds->status;
+        if ((rc = cuda_rc(launch_parts_tc(pp, mk, mv, stream)))) return rc;
+        ++t_launches;
+        ScanParams sp{};
+        sp.rec = wsf, sp.base_M = M_in, sp.base_z = z_in, sp.BH = (int)BH, sp.nch = (int)nch;
+        sp.d = d, sp.dv = dv_dim, sp.len = rec, sp.reverse = false;
+        if ((rc = cuda_rc(launch_scan_states(sp, stream)))) return rc;
+        ++t_launches;
+        BwdTcParams tp{};
+        tp.dq = dq, tp.dk = dk, tp.dv = dv, tp.states = wsf, tp.rev = wsf + off_rev, tp.G = G, tp.E = wsf + off_E;
+        tp.B = B, tp.H = H, tp.T = T, tp.d = d, tp.dv_dim = dv_dim, tp.nch = (int)nch, tp.rec = rec, tp.eps = eps;
+        tp.status = ds->status;
+        if ((rc = cuda_rc(launch_bwd_dq_tc(tp, mq, mk, mv, mdo, stream)))) return rc;
+        ++t_launches;
+        ScanParams rp{};
+        rp.rec = wsf + off_rev, rp.base_M = dM_out, rp.base_z = dz_out, rp.total_M = dM_in, rp.total_z = dz_in;
+        rp.BH = (int)BH, rp.nch = (int)nch, rp.d = d, rp.dv = dv_dim, rp.len = rec, rp.reverse = true;
+        if ((rc = cuda_rc(launch_scan_states(rp, stream)))) return rc;
+        ++t_launches;
+        if ((rc = cuda_rc(launch_bwd_dkdv_tc(tp, mq, mk, mv, mg, stream)))) return rc;
+        ++t_launches;
+        return LA_OK;
+    }
 
     BwdParams bp{};
     bp.q = q, bp.k = k, bp.v = v, bp.dout = dout, bp.dq = dq, bp.dk = dk, bp.dv = dv;
@@ -540,6 +621,34 @@ int la_causal_fwd_ex(const void* q, const void* k, const void* v, void* out, con
                     workspace_bytes, false, (cudaStream_t)stream);
 }
 
+int la_causal_fwd_mapped(const void* q, const void* k, const void* v, void* out, const float* M_in,
+                         const float* z_in, float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv,
+                         int chunk, float eps, la_dtype dtype, const int64_t* strides, void* workspace,
+                         size_t workspace_bytes, la_stream_t stream) {
+    return fwd_impl(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chunk, eps, dtype, strides, workspace,
+                    workspace_bytes, false, (cudaStream_t)stream, true);
+}
+
+int la_feature_map_prf(const void* x, const void* W, void* out, int64_t rows, int d, int m, la_dtype dtype,
+                       la_stream_t stream) {
+    t_launches = 0;
+    if (!x || !W || !out || rows <= 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_BF16 || (d != 64 && d != 128) || (m != 64 && m != 128)) return LA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(out)) return LA_ERR_INVALID_ARG;
+    if (out == x || out == W) return LA_ERR_INVALID_ARG;
+    if (rows >= (int64_t(1) << 31)) return LA_ERR_UNSUPPORTED;
+    DeviceState* ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc) return rc;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, d, rows, 1, 1, d, rows * d, rows * d) || !make_map(&mw, W, d, m, 1, 1, d, (int64_t)m * d,
+                                                                           (int64_t)m * d))
+        return LA_ERR_CUDA;
+    rc = cuda_rc(launch_fmap_prf(mx, mw, out, rows, d, m, ds->status, (cudaStream_t)stream));
+    if (!rc) ++t_launches;
+    return rc;
+}
+
 size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int chunk, la_dtype dtype) {
     if (B <= 0 || H <= 0 || T <= 0 || !shape_ok(d, dv)) return 0;
     int sm = 148;
@@ -584,6 +693,8 @@ int la_decode_step(const void* q, const void* k, const void* v, void* out, float
     if (rc) return rc;
     DecodeParams p{};
     p.q = q, p.k = k, p.v = v, p.out = out, p.M = M, p.z = z, p.N = N, p.H = H, p.d = d, p.dv = dv, p.eps = eps;
+    // extents: one token per (stream, head); the state [N, H, d, dv] and [N, H, d]
+    p.ext = make_extents(N, H, 1, d, dv, contiguous(H, 1, d, dv), 0), p.status = ds->status;
     rc = cuda_rc(launch_decode(p, dtype == LA_BF16, (cudaStream_t)stream));
     if (!rc) ++t_launches;
     return rc;
@@ -632,7 +743,8 @@ int la_get_last_device_status(la_stream_t stream) {
         const int zero = 0;
         if (cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return LA_ERR_CUDA;
     }
-    return (v & STATUS_TIMEOUT) ? LA_ERR_TIMEOUT : LA_OK;
+    if (v & STATUS_TIMEOUT) return LA_ERR_TIMEOUT;
+    return (v & STATUS_BOUNDS) ? LA_ERR_BOUNDS : LA_OK;
 }
 
 const char* la_get_error_string(int code) {
@@ -644,10 +756,13 @@ const char* la_get_error_string(int code) {
         case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
         case LA_ERR_WORKSPACE: return "workspace pointer not 256-byte aligned, or too small for a call that needs one";
         case LA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's static buffer holds";
+        case LA_ERR_BOUNDS: return "checked build: a kernel access fell outside a buffer's extent and was skipped";
         default: return "unknown error";
     }
 }
 
 int la_last_launch_count(void) { return t_launches; }
+
+int la_checked_build(void) { return LA_CHECKS; }
 
 }  // extern "C"

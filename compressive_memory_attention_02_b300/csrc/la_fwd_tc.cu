@@ -523,8 +523,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (!ok) break;
             const int64_t t0 = (int64_t)(is_main ? main_begin + g - n_agg : g) * CH;
             const int valid = (int)min64(CH, p.T - t0);
-            if (is_main) phi_tile<D, 32 * NFW>(sm + L::Q0 + s * L::QB, ATOM, CH, ct, nullptr);
-            phi_tile<D, 32 * NFW>(sm + L::K0 + s * L::KB, ATOMK, valid, ct, nullptr);
+            if (is_main) phi_tile<D, 32 * NFW>(sm + L::Q0 + s * L::QB, ATOM, CH, ct, nullptr, p.phi_ident);
+            phi_tile<D, 32 * NFW>(sm + L::K0 + s * L::KB, ATOMK, valid, ct, nullptr, p.phi_ident);
             fence_proxy_async_smem();
             named_bar_sync(1, 32 * NFW);
             if (ct == 0) mbar_arrive(&phib[s]);

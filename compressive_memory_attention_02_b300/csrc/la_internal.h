@@ -9,7 +9,24 @@
 #include "../../include/linattn.h"
 #include "la_ptx.cuh"
 
+// LA_CHECKS=1 builds the checked library: every global-memory access of the SIMT, reduce,
+// read-out and decode kernels is tested against the extent of the caller's buffer first;
+// an access outside it is skipped and STATUS_BOUNDS is recorded in the device status word
+// (read back by la_get_last_device_status as LA_ERR_BOUNDS). Nothing traps. The tensor-core
+// kernels' tiles are bounded by their tensor maps either way.
+#ifndef LA_CHECKS
+#define LA_CHECKS 0
+#endif
+
 namespace la {
+
+// Element counts of the buffers a SIMT kernel may touch, for the checked build: q, k, v,
+// out (strided spans), the initial and final state, and the workspace records.
+struct Extents {
+    int64_t q, k, v, o;
+    int64_t M_in, z_in, M_out, z_out;
+    int64_t ws;
+};
 
 // Element strides (innermost stride is 1) of q, k, v and out in [B, H, T, .].
 struct Strides {
@@ -33,6 +50,9 @@ struct FwdParams {
     int d, dv, chunk;
     float eps;
     Strides st;
+    Extents ext;
+    int* status;
+    int phi_ident;         // q, k hold feature values already (no elu + 1)
 };
 
 // Per-part state sums. Record (bh, p) is at dst_M + (bh*nparts + p)*rec_M (d x dv,
@@ -54,7 +74,9 @@ struct PartsParams {
     int nparts;
     float eps;
     Strides st;
+    Extents ext;           // M_out / z_out: the extents of dst_M / dst_z, records or state
     int* status;
+    int phi_ident;         // k (and q) hold feature values already (no elu + 1)
 };
 
 struct ReduceParams {
@@ -66,6 +88,8 @@ struct ReduceParams {
     float* dst_M;
     float* dst_z;
     int BH, d, dv, nparts;
+    Extents ext;           // ws: the part records
+    int* status;
 };
 
 struct PrefillOutParams {
@@ -78,6 +102,8 @@ struct PrefillOutParams {
     int d, dv;
     float eps;
     Strides st;
+    Extents ext;           // M_out, z_out: the final state read here
+    int* status;
 };
 
 struct DecodeParams {
@@ -89,6 +115,8 @@ struct DecodeParams {
     float* z;
     int N, H, d, dv;
     float eps;
+    Extents ext;           // q, k, v, o: the token tensors; M_out, z_out: the state
+    int* status;
 };
 
 // Tensor-core forward: one block per (range, b*H + h). Range r processes the main
@@ -110,10 +138,24 @@ struct FwdTcParams {
     int64_t T;
     float eps;
     int* status;
+    int phi_ident;         // q, k hold feature values already (no elu + 1)
 };
 
 // device status word bits
-enum : int { STATUS_TIMEOUT = 1 };
+enum : int { STATUS_TIMEOUT = 1, STATUS_BOUNDS = 2 };
+
+// Checked build: true iff elements [i, i + n) lie inside [0, len); otherwise STATUS_BOUNDS
+// is recorded and the caller skips the access. The normal build compiles this to true.
+__device__ __forceinline__ bool inb(int64_t i, int64_t n, int64_t len, int* status) {
+#if LA_CHECKS
+    if (i >= 0 && i + n <= len) return true;
+    if (status) atomicOr(status, STATUS_BOUNDS);
+    return false;
+#else
+    (void)i, (void)n, (void)len, (void)status;
+    return true;
+#endif
+}
 
 // SIMT launchers (la_simt.cu)
 size_t fwd_simt_smem(int d, int dv, int C);
@@ -129,6 +171,11 @@ cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_parts_tc(const PartsParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s);
+
+// Positive random-feature map (la_fmap.cu): maps {d, rows} over x [rows, d] and {d, m} over
+// W [m, d], both bf16; out [rows, m] bf16.
+cudaError_t launch_fmap_prf(const CUtensorMap& mx, const CUtensorMap& mw, void* out, int64_t rows, int d, int m,
+                            int* status, cudaStream_t s);
 
 // Device address of the current device's status word (la_api.cu).
 int device_status_word(int** status);

@@ -37,6 +37,9 @@ __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p, float x) {
     *p = __float2bfloat16_rn(x);
 }
 
+// phi = elu + 1, or the value itself when q and k hold feature values already
+__device__ __forceinline__ float phi_x(float x, int ident) { return ident ? x : phi_f(x); }
+
 // ------------------------------------------------------------------ forward
 // One block per (b, h). Shared memory (float): M[d*dv] z[d] Q[C*d] K[C*d] V[C*dv] S[C*C] den[C].
 template <typename TI>
@@ -53,13 +56,23 @@ __global__ void __launch_bounds__(256) fwd_simt_kernel(FwdParams p) {
     float* Vs = Ks + C * d;
     float* Ss = Vs + C * dv;
     float* ds = Ss + C * C;
-    const TI* q = static_cast<const TI*>(p.q) + b * p.st.q_sb + h * p.st.q_sh;
-    const TI* k = static_cast<const TI*>(p.k) + b * p.st.k_sb + h * p.st.k_sh;
-    const TI* v = static_cast<const TI*>(p.v) + b * p.st.v_sb + h * p.st.v_sh;
-    TI* o = static_cast<TI*>(p.out) + b * p.st.o_sb + h * p.st.o_sh;
+    // element offsets of this head in q, k, v, out (every access is checked against the
+    // buffer's extent in the checked build)
+    const TI* q = static_cast<const TI*>(p.q);
+    const TI* k = static_cast<const TI*>(p.k);
+    const TI* v = static_cast<const TI*>(p.v);
+    TI* o = static_cast<TI*>(p.out);
+    const int64_t qh = b * p.st.q_sb + h * p.st.q_sh, kh = b * p.st.k_sb + h * p.st.k_sh;
+    const int64_t vh = b * p.st.v_sb + h * p.st.v_sh, oh = b * p.st.o_sb + h * p.st.o_sh;
 
-    for (int i = tid; i < d * dv; i += nt) Ms[i] = p.M_in ? p.M_in[(int64_t)bh * d * dv + i] : 0.f;
-    for (int i = tid; i < d; i += nt) zs[i] = p.z_in ? p.z_in[(int64_t)bh * d + i] : 0.f;
+    for (int i = tid; i < d * dv; i += nt) {
+        const int64_t e = (int64_t)bh * d * dv + i;
+        Ms[i] = p.M_in && inb(e, 1, p.ext.M_in, p.status) ? p.M_in[e] : 0.f;
+    }
+    for (int i = tid; i < d; i += nt) {
+        const int64_t e = (int64_t)bh * d + i;
+        zs[i] = p.z_in && inb(e, 1, p.ext.z_in, p.status) ? p.z_in[e] : 0.f;
+    }
 
     for (int64_t c0 = 0; c0 < p.T; c0 += C) {
         const int n = (int)min64(C, p.T - c0);
@@ -68,15 +81,17 @@ __global__ void __launch_bounds__(256) fwd_simt_kernel(FwdParams p) {
             const int t = idx / d, i = idx % d;
             float qf = 0.f, kf = 0.f;
             if (t < n) {
-                qf = phi_f(ldf(q + (c0 + t) * p.st.q_st + i));
-                kf = phi_f(ldf(k + (c0 + t) * p.st.k_st + i));
+                const int64_t iq = qh + (c0 + t) * p.st.q_st + i, ik = kh + (c0 + t) * p.st.k_st + i;
+                if (inb(iq, 1, p.ext.q, p.status)) qf = phi_x(ldf(q + iq), p.phi_ident);
+                if (inb(ik, 1, p.ext.k, p.status)) kf = phi_x(ldf(k + ik), p.phi_ident);
             }
             Qs[idx] = qf;
             Ks[idx] = kf;  // rows past the end stay 0: phi of padding must not enter z
         }
         for (int idx = tid; idx < C * dv; idx += nt) {
             const int t = idx / dv, j = idx % dv;
-            Vs[idx] = (t < n) ? ldf(v + (c0 + t) * p.st.v_st + j) : 0.f;
+            const int64_t iv = vh + (c0 + t) * p.st.v_st + j;
+            Vs[idx] = (t < n && inb(iv, 1, p.ext.v, p.status)) ? ldf(v + iv) : 0.f;
         }
         __syncthreads();
         // intra-chunk scores, lower triangle with diagonal
@@ -107,7 +122,8 @@ __global__ void __launch_bounds__(256) fwd_simt_kernel(FwdParams p) {
             const float* qr = Qs + t * d;
             for (int i = 0; i < d; ++i) inter = fmaf(qr[i], Ms[i * dv + j], inter);
             for (int s = 0; s <= t; ++s) intra = fmaf(Ss[t * C + s], Vs[s * dv + j], intra);
-            stf(o + (c0 + t) * p.st.o_st + j, (inter + intra) / ds[t]);
+            const int64_t io = oh + (c0 + t) * p.st.o_st + j;
+            if (inb(io, 1, p.ext.o, p.status)) stf(o + io, (inter + intra) / ds[t]);
         }
         __syncthreads();
         // state update: M += phi(K)^T V, z += sum phi(K)
@@ -125,9 +141,15 @@ __global__ void __launch_bounds__(256) fwd_simt_kernel(FwdParams p) {
     }
     __syncthreads();
     if (p.M_out)
-        for (int i = tid; i < d * dv; i += nt) p.M_out[(int64_t)bh * d * dv + i] = Ms[i];
+        for (int i = tid; i < d * dv; i += nt) {
+            const int64_t e = (int64_t)bh * d * dv + i;
+            if (inb(e, 1, p.ext.M_out, p.status)) p.M_out[e] = Ms[i];
+        }
     if (p.z_out)
-        for (int i = tid; i < d; i += nt) p.z_out[(int64_t)bh * d + i] = zs[i];
+        for (int i = tid; i < d; i += nt) {
+            const int64_t e = (int64_t)bh * d + i;
+            if (inb(e, 1, p.ext.z_out, p.status)) p.z_out[e] = zs[i];
+        }
 }
 
 // ------------------------------------------------------------------ per-part state sums
@@ -150,8 +172,9 @@ __global__ void __launch_bounds__(256) parts_simt_kernel(PartsParams p) {
     float* Ks = ss + d;
     float* Vs = Ks + TILE * d;
     float* fq = Vs + TILE * dv;
-    const TI* k = static_cast<const TI*>(p.k) + b * p.st.k_sb + h * p.st.k_sh;
-    const TI* v = static_cast<const TI*>(p.v) + b * p.st.v_sb + h * p.st.v_sh;
+    const TI* k = static_cast<const TI*>(p.k);
+    const TI* v = static_cast<const TI*>(p.v);
+    const int64_t kh = b * p.st.k_sb + h * p.st.k_sh, vh = b * p.st.v_sb + h * p.st.v_sh;
     const int64_t t_begin = (int64_t)part * p.part_len;
     const int64_t t_end = min64(p.T, t_begin + p.part_len);
 
@@ -162,11 +185,13 @@ __global__ void __launch_bounds__(256) parts_simt_kernel(PartsParams p) {
         __syncthreads();
         for (int idx = tid; idx < TILE * d; idx += nt) {
             const int t = idx / d, i = idx % d;
-            Ks[idx] = (t < n) ? phi_f(ldf(k + (t0 + t) * p.st.k_st + i)) : 0.f;
+            const int64_t ik = kh + (t0 + t) * p.st.k_st + i;
+            Ks[idx] = (t < n && inb(ik, 1, p.ext.k, p.status)) ? phi_x(ldf(k + ik), p.phi_ident) : 0.f;
         }
         for (int idx = tid; idx < TILE * dv; idx += nt) {
             const int t = idx / dv, j = idx % dv;
-            Vs[idx] = (t < n) ? ldf(v + (t0 + t) * p.st.v_st + j) : 0.f;
+            const int64_t iv = vh + (t0 + t) * p.st.v_st + j;
+            Vs[idx] = (t < n && inb(iv, 1, p.ext.v, p.status)) ? ldf(v + iv) : 0.f;
         }
         __syncthreads();
         for (int idx = tid; idx < d * dv; idx += nt) {
@@ -183,26 +208,41 @@ __global__ void __launch_bounds__(256) parts_simt_kernel(PartsParams p) {
     }
     __syncthreads();
     if (p.base_M)
-        for (int i = tid; i < d * dv; i += nt) As[i] += p.base_M[(int64_t)bh * d * dv + i];
+        for (int i = tid; i < d * dv; i += nt) {
+            const int64_t e = (int64_t)bh * d * dv + i;
+            if (inb(e, 1, p.ext.M_in, p.status)) As[i] += p.base_M[e];
+        }
     if (p.base_z)
-        for (int i = tid; i < d; i += nt) ss[i] += p.base_z[(int64_t)bh * d + i];
+        for (int i = tid; i < d; i += nt) {
+            const int64_t e = (int64_t)bh * d + i;
+            if (inb(e, 1, p.ext.z_in, p.status)) ss[i] += p.base_z[e];
+        }
     __syncthreads();
     const int64_t rec = (int64_t)bh * p.nparts + part;
     if (p.dst_M)
-        for (int i = tid; i < d * dv; i += nt) p.dst_M[rec * p.rec_M + i] = As[i];
+        for (int i = tid; i < d * dv; i += nt) {
+            const int64_t e = rec * p.rec_M + i;
+            if (inb(e, 1, p.ext.M_out, p.status)) p.dst_M[e] = As[i];
+        }
     if (p.dst_z)
-        for (int i = tid; i < d; i += nt) p.dst_z[rec * p.rec_z + i] = ss[i];
+        for (int i = tid; i < d; i += nt) {
+            const int64_t e = rec * p.rec_z + i;
+            if (inb(e, 1, p.ext.z_out, p.status)) p.dst_z[e] = ss[i];
+        }
     if (p.out_last) {  // only launched with nparts == 1
-        const TI* q = static_cast<const TI*>(p.q) + b * p.st.q_sb + h * p.st.q_sh + (p.T - 1) * p.st.q_st;
-        for (int i = tid; i < d; i += nt) fq[i] = phi_f(ldf(q + i));
+        const TI* q = static_cast<const TI*>(p.q);
+        const int64_t qt = b * p.st.q_sb + h * p.st.q_sh + (p.T - 1) * p.st.q_st;
+        for (int i = tid; i < d; i += nt)
+            fq[i] = inb(qt + i, 1, p.ext.q, p.status) ? phi_x(ldf(q + qt + i), p.phi_ident) : 0.f;
         __syncthreads();
         float den = p.eps;
         for (int i = 0; i < d; ++i) den = fmaf(fq[i], ss[i], den);
-        TI* o = static_cast<TI*>(p.out_last) + (int64_t)bh * dv;
+        TI* o = static_cast<TI*>(p.out_last);
         for (int j = tid; j < dv; j += nt) {
             float num = 0.f;
             for (int i = 0; i < d; ++i) num = fmaf(fq[i], As[i * dv + j], num);
-            stf(o + j, num / den);
+            const int64_t e = (int64_t)bh * dv + j;
+            if (inb(e, 1, p.ext.o, p.status)) stf(o + e, num / den);
         }
     }
 }
@@ -219,22 +259,26 @@ __global__ void __launch_bounds__(256) reduce_parts_kernel(ReduceParams p) {
     const int e = e4 * 4;
     const bool isM = e < dd;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t se = isM ? (int64_t)bh * dd + e : (int64_t)bh * p.d + (e - dd);  // state element
     if (isM ? (p.base_M != nullptr) : (p.base_z != nullptr)) {
-        const float* src = isM ? p.base_M + (int64_t)bh * dd + e : p.base_z + (int64_t)bh * p.d + (e - dd);
-        acc = *reinterpret_cast<const float4*>(src);
+        const float* src = isM ? p.base_M : p.base_z;
+        if (inb(se, 4, isM ? p.ext.M_in : p.ext.z_in, p.status)) acc = *reinterpret_cast<const float4*>(src + se);
     }
+    // part records: parts_M / parts_z are the M and z views of one record array of p.ext.ws
+    // floats that starts at parts_M
     const float* part = isM ? p.parts_M + (int64_t)bh * p.nparts * p.rec_M + e
                             : p.parts_z + (int64_t)bh * p.nparts * p.rec_z + (e - dd);
     const int64_t stride = isM ? p.rec_M : p.rec_z;
     for (int i = 0; i < p.nparts; ++i) {
+        if (!inb((part + i * stride) - p.parts_M, 4, p.ext.ws, p.status)) continue;
         const float4 x = *reinterpret_cast<const float4*>(part + i * stride);
         acc.x += x.x;
         acc.y += x.y;
         acc.z += x.z;
         acc.w += x.w;
     }
-    float* dst = isM ? p.dst_M + (int64_t)bh * dd + e : p.dst_z + (int64_t)bh * p.d + (e - dd);
-    *reinterpret_cast<float4*>(dst) = acc;
+    float* dst = isM ? p.dst_M : p.dst_z;
+    if (inb(se, 4, isM ? p.ext.M_out : p.ext.z_out, p.status)) *reinterpret_cast<float4*>(dst + se) = acc;
 }
 
 // ------------------------------------------------------------------ last-token read-out
@@ -245,21 +289,27 @@ __global__ void __launch_bounds__(128) prefill_out_kernel(PrefillOutParams p) {
     __shared__ float red[4];
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int tid = threadIdx.x;
-    const TI* q = static_cast<const TI*>(p.q) + b * p.st.q_sb + h * p.st.q_sh + (p.T - 1) * p.st.q_st;
+    const TI* q = static_cast<const TI*>(p.q);
+    const int64_t qt = b * p.st.q_sb + h * p.st.q_sh + (p.T - 1) * p.st.q_st;
     float part = 0.f;
     if (tid < p.d) {
-        fq[tid] = phi_f(ldf(q + tid));
-        part = fq[tid] * p.z[(int64_t)bh * p.d + tid];
+        const int64_t ez = (int64_t)bh * p.d + tid;
+        fq[tid] = inb(qt + tid, 1, p.ext.q, p.status) ? phi_f(ldf(q + qt + tid)) : 0.f;
+        part = inb(ez, 1, p.ext.z_out, p.status) ? fq[tid] * p.z[ez] : 0.f;
     }
     for (int off = 16; off; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
     if ((tid & 31) == 0) red[tid >> 5] = part;
     __syncthreads();
     const float den = red[0] + red[1] + red[2] + red[3] + p.eps;
-    const float* M = p.M + (int64_t)bh * p.d * p.dv;
+    const int64_t mh = (int64_t)bh * p.d * p.dv;
     for (int j = tid; j < p.dv; j += blockDim.x) {
         float num = 0.f;
-        for (int i = 0; i < p.d; ++i) num = fmaf(fq[i], M[i * p.dv + j], num);
-        stf(static_cast<TI*>(p.out) + (int64_t)bh * p.dv + j, num / den);
+        for (int i = 0; i < p.d; ++i) {
+            const int64_t e = mh + (int64_t)i * p.dv + j;
+            if (inb(e, 1, p.ext.M_out, p.status)) num = fmaf(fq[i], p.M[e], num);
+        }
+        const int64_t eo = (int64_t)bh * p.dv + j;
+        if (inb(eo, 1, p.ext.o, p.status)) stf(static_cast<TI*>(p.out) + eo, num / den);
     }
 }
 
@@ -292,28 +342,33 @@ __global__ void __launch_bounds__(DEC_NT, 3) decode_kernel(DecodeParams p) {
     const int cg = tid % ncg, rg = tid / ncg;
     const int nrows = rg < R ? (d - rg + R - 1) / R : 0;  // rows rg, rg+R, ... < d (threads past R*ncg idle)
     const int rs4 = dv >> 2;                               // row stride of M in float4
-    float4* M4 = reinterpret_cast<float4*>(p.M + (int64_t)nh * d * dv + c0) + cg;
+    const int64_t m0 = (int64_t)nh * d * dv + c0 + 4 * cg;  // element of M at (row 0, this column group)
+    float4* M4 = reinterpret_cast<float4*>(p.M + m0);
     float4 m[MAXR];
 #pragma unroll
     for (int r = 0; r < MAXR; ++r)
-        if (r < nrows) m[r] = __ldcs(M4 + (int64_t)(rg + r * R) * rs4);
+        if (r < nrows && inb(m0 + (int64_t)(rg + r * R) * dv, 4, p.ext.M_out, p.status))
+            m[r] = __ldcs(M4 + (int64_t)(rg + r * R) * rs4);
+        else
+            m[r] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-    const TI* q = static_cast<const TI*>(p.q) + (int64_t)nh * d;
-    const TI* k = static_cast<const TI*>(p.k) + (int64_t)nh * d;
-    const TI* v = static_cast<const TI*>(p.v) + (int64_t)nh * dv + c0;
+    const TI* q = static_cast<const TI*>(p.q);
+    const TI* k = static_cast<const TI*>(p.k);
+    const TI* v = static_cast<const TI*>(p.v);
+    const int64_t qk0 = (int64_t)nh * d, v0 = (int64_t)nh * dv + c0;
     float zo = 0.f;
     if (tid < d) {
-        zo = p.z[(int64_t)nh * d + tid];
-        fq[tid] = phi_f(ldf(q + tid));
-        fk[tid] = phi_f(ldf(k + tid));
+        if (inb(qk0 + tid, 1, p.ext.z_out, p.status)) zo = p.z[qk0 + tid];
+        fq[tid] = inb(qk0 + tid, 1, p.ext.q, p.status) ? phi_f(ldf(q + qk0 + tid)) : 0.f;
+        fk[tid] = inb(qk0 + tid, 1, p.ext.k, p.status) ? phi_f(ldf(k + qk0 + tid)) : 0.f;
     }
-    if (tid < width) vv[tid] = ldf(v + tid);
+    if (tid < width) vv[tid] = inb(v0 + tid, 1, p.ext.v, p.status) ? ldf(v + v0 + tid) : 0.f;
     __syncthreads();
     // z <- z + phi(k) (written by the first column block); den = phi(q) . z + eps
     float part = 0.f;
     if (tid < d) {
         const float zn = zo + fk[tid];
-        if (blockIdx.y == 0) p.z[(int64_t)nh * d + tid] = zn;
+        if (blockIdx.y == 0 && inb(qk0 + tid, 1, p.ext.z_out, p.status)) p.z[qk0 + tid] = zn;
         part = fq[tid] * zn;
     }
     for (int off = 16; off; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
@@ -331,7 +386,7 @@ __global__ void __launch_bounds__(DEC_NT, 3) decode_kernel(DecodeParams p) {
             x.y = fmaf(a, v4.y, x.y);
             x.z = fmaf(a, v4.z, x.z);
             x.w = fmaf(a, v4.w, x.w);
-            __stcs(M4 + (int64_t)i * rs4, x);
+            if (inb(m0 + (int64_t)i * dv, 4, p.ext.M_out, p.status)) __stcs(M4 + (int64_t)i * rs4, x);
             acc.x = fmaf(g, x.x, acc.x);
             acc.y = fmaf(g, x.y, acc.y);
             acc.z = fmaf(g, x.z, acc.z);
@@ -351,11 +406,14 @@ __global__ void __launch_bounds__(DEC_NT, 3) decode_kernel(DecodeParams p) {
         }
         float den = p.eps;
         for (int w = 0; w < 4; ++w) den += dred[w];  // threads >= d (<= 128) add nothing
-        TI* o = static_cast<TI*>(p.out) + (int64_t)nh * dv + c0 + tid * 4;
-        stf(o + 0, s.x / den);
-        stf(o + 1, s.y / den);
-        stf(o + 2, s.z / den);
-        stf(o + 3, s.w / den);
+        const int64_t eo = (int64_t)nh * dv + c0 + tid * 4;
+        TI* o = static_cast<TI*>(p.out) + eo;
+        if (inb(eo, 4, p.ext.o, p.status)) {
+            stf(o + 0, s.x / den);
+            stf(o + 1, s.y / den);
+            stf(o + 2, s.z / den);
+            stf(o + 3, s.w / den);
+        }
     }
 }
 

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(PARTS_THREADS, 2)
             ok = bar_and(1, NT, mbar_wait(&full[s], (c / NS) & 1, abort_flag));
             if (!ok) break;
             const int valid = (int)min64(CH, t_end - (t_begin + (int64_t)c * CH));
-            phi_tile<D, NT>(sm + s * L::STAGE, ATOM, valid, ct, colsum);
+            phi_tile<D, NT>(sm + s * L::STAGE, ATOM, valid, ct, colsum, p.phi_ident);
             fence_proxy_async_smem();
             named_bar_sync(1, NT);
             if (ct == 0) mbar_arrive(&phib[s]);

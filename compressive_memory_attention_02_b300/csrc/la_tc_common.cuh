@@ -69,10 +69,13 @@ __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
 // (g = ct / (D/8)); since RG is a multiple of 8 the swizzled chunk position
 // j ^ (row % 8) is the same for all of its rows. Rows >= valid become 0 (phi(0) = 1
 // must not enter the sums; pass valid = 64 to keep all rows). With colsum != nullptr
-// the thread adds the bf16-rounded results of its 8 columns into colsum[0..8).
+// the thread adds the bf16-rounded results of its 8 columns into colsum[0..8). With
+// ident the tile already holds feature values (another map applied by the caller): rows
+// below valid are kept as they are, the others still become 0.
 // The row loop is unrolled so that a thread's rows are in flight together.
 template <int D, int NT = 128>
-__device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, int ct, float* colsum) {
+__device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, int ct, float* colsum,
+                                         bool ident = false) {
     constexpr int CPR = D / 8;
     constexpr int RG = NT / CPR;
     static_assert(RG % 8 == 0, "rows of a thread share one swizzle phase");
@@ -90,8 +93,10 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int astride, int valid, 
         uint4 x = base[i * RG * 8];
         uint32_t w[4] = {x.x, x.y, x.z, x.w};
         if (g + i * RG < valid) {
+            if (!ident) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = phi_bf16x2(w[e]);
+                for (int e = 0; e < 4; ++e) w[e] = phi_bf16x2(w[e]);
+            }
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) w[e] = 0u;

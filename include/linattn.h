@@ -64,8 +64,10 @@ enum {
     LA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
     LA_ERR_TIMEOUT = 4,       /* device status: a bounded wait inside a kernel ran out */
     LA_ERR_WORKSPACE = 5,     /* workspace pointer misaligned, or too small for la_causal_bwd */
-    LA_ERR_SCRATCH_LIMIT = 6  /* la_prefill_state_noalloc: the problem needs more scratch than
+    LA_ERR_SCRATCH_LIMIT = 6, /* la_prefill_state_noalloc: the problem needs more scratch than
                                  LA_NOALLOC_SCRATCH_BYTES */
+    LA_ERR_BOUNDS = 7         /* device status, checked build only: an access outside a buffer's
+                                 extent was found and skipped */
 };
 
 /* ---- training forward (mode 3 of the mode table: all outputs) -------------
@@ -102,6 +104,32 @@ int la_causal_fwd_ex(const void* q, const void* k, const void* v, void* out,
 
 size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int chunk,
                                     la_dtype dtype);
+
+/* ---- other feature maps ------------------------------------------------------
+ * The page "Attention_Kernel_Mask" lists positive random features (PRF) and orthogonal
+ * random features (ORF) among the feature maps of its non-causal kernel discussion,
+ * without printing them. They run through the same chunked kernels in two steps:
+ *
+ * la_feature_map_prf: out[r] = exp(W x_r - |x_r|^2 / 2) / sqrt(m) for every row r, the
+ * positive random-feature map (ORF: the same map with rows of W orthogonal within blocks
+ * of d, built by the caller). Tensor cores; bf16 only.
+ *   x    [rows, d] bf16, contiguous rows (for q or k: rows = B*H*T), 16-byte aligned, read
+ *   W    [m, d] bf16, 16-byte aligned, read
+ *   out  [rows, m] bf16, written; must not alias x or W
+ *   d, m in {64, 128}; otherwise LA_ERR_UNSUPPORTED.
+ *
+ * la_causal_fwd_mapped: la_causal_fwd_ex with q and k holding feature values already
+ * (phi(q), phi(k) of any map, nonnegative for a positive denominator): the same
+ * computation with the map applied by the caller instead of elu + 1; d is the feature
+ * count. Same arguments, layouts and errors as la_causal_fwd_ex. */
+int la_feature_map_prf(const void* x, const void* W, void* out, int64_t rows, int d, int m,
+                       la_dtype dtype, la_stream_t stream);
+
+int la_causal_fwd_mapped(const void* q, const void* k, const void* v, void* out,
+                         const float* M_in, const float* z_in, float* M_out, float* z_out,
+                         int B, int H, int64_t T, int d, int dv, int chunk, float eps,
+                         la_dtype dtype, const int64_t* strides,
+                         void* workspace, size_t workspace_bytes, la_stream_t stream);
 
 /* ---- prefill (prompt mode: state plus last output) ---------------------------
  * Only the final state and the last token's output, as the mode table's note
@@ -218,7 +246,8 @@ size_t la_causal_bwd_workspace_size(int B, int H, int64_t T, int d, int dv);
 int la_set_workspace(void* ptr, size_t bytes);
 
 /* Reads and clears this device's status word; synchronises `stream` first.
- * Returns LA_OK or the first device-side error recorded since the last read. */
+ * Returns LA_OK, or the device-side error recorded since the last read (LA_ERR_TIMEOUT
+ * before LA_ERR_BOUNDS when both were). */
 int la_get_last_device_status(la_stream_t stream);
 
 const char* la_get_error_string(int code);
@@ -233,6 +262,13 @@ int la_selftest_wait_timeout(unsigned long long limit_cycles, la_stream_t stream
 
 /* Number of kernels the most recent call on this host thread launched. */
 int la_last_launch_count(void);
+
+/* 1 in the checked library (liblinattn_checked.so, built with LA_CHECKS=1), 0 otherwise. The
+ * checked library tests every global-memory access of its SIMT, reduce, read-out and decode
+ * kernels against the extent of the caller's buffer (from the shapes and strides given);
+ * an access outside it is skipped and recorded, and la_get_last_device_status then returns
+ * LA_ERR_BOUNDS. It is a debugging build: slower, same results otherwise. */
+int la_checked_build(void);
 
 #ifdef __cplusplus
 }

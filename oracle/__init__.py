@@ -24,6 +24,9 @@ Contents
                                        split of D_t is our reading)
   noncausal                            all-token (non-causal) linear attention
   phi                                  elu(x) + 1
+  phi_prf / orf_matrix                 positive (and orthogonal) random features, used
+                                       with phi="identity": the recurrence on feature
+                                       values given by the caller
   rel_err_rows / rel_err_state         the tolerance metrics
 
 Readings taken where the pages are silent or garbled:
@@ -65,10 +68,10 @@ def _load():
         lib = ctypes.CDLL(build())
         i64, c_int, vp, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double
         lib.oracle_causal_fwd.argtypes = [vp, vp, vp, c_int, vp, vp, vp, vp, vp,
-                                          i64, i64, i64, c_int, c_int, dbl, c_int]
+                                          i64, i64, i64, c_int, c_int, dbl, c_int, c_int]
         lib.oracle_prefill.argtypes = lib.oracle_causal_fwd.argtypes
         lib.oracle_decode_step.argtypes = [vp, vp, vp, c_int, vp, vp, vp,
-                                           i64, i64, c_int, c_int, dbl, c_int]
+                                           i64, i64, c_int, c_int, dbl, c_int, c_int]
         lib.oracle_phi.argtypes = [vp, vp, i64]
         lib.oracle_causal_bwd.argtypes = [vp, vp, vp, c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                           i64, i64, i64, c_int, c_int, dbl, c_int]
@@ -89,7 +92,18 @@ def _dtype_code(a: np.ndarray) -> int:
         return 1
     if a.dtype == np.float32:
         return 0
-    raise TypeError("storage arrays are uint16 (bf16 bits) or float32")
+    if a.dtype == np.float64:
+        return 2
+    raise TypeError("storage arrays are uint16 (bf16 bits), float32 or float64")
+
+
+_PHI = {"elu1": 0, "identity": 1}
+
+
+def _phi_kind(phi):
+    """'elu1': phi = elu + 1 applied to q and k; 'identity': q and k are feature values
+    already (another feature map applied by the caller)."""
+    return _PHI[phi]
 
 
 def _c(a):
@@ -108,9 +122,9 @@ def _state_or_none(a, shape):
     return a
 
 
-def causal_fwd(q, k, v, M_in=None, z_in=None, eps=1e-6, want_out=True, mutation=0):
-    """All outputs and the final state. q, k: [B,H,T,d]; v: [B,H,T,dv] storage arrays.
-    Returns (out [B,H,T,dv] float64 or None, M [B,H,d,dv], z [B,H,d])."""
+def causal_fwd(q, k, v, M_in=None, z_in=None, eps=1e-6, want_out=True, mutation=0, phi="elu1"):
+    """All outputs and the final state. q, k: [B,H,T,d]; v: [B,H,T,dv] storage arrays
+    (the same dtype). Returns (out [B,H,T,dv] float64 or None, M [B,H,d,dv], z [B,H,d])."""
     q, k, v = _c(q), _c(k), _c(v)
     assert q.dtype == k.dtype == v.dtype
     B, H, T, d = q.shape
@@ -123,11 +137,11 @@ def causal_fwd(q, k, v, M_in=None, z_in=None, eps=1e-6, want_out=True, mutation=
     z = np.empty((B, H, d))
     _load().oracle_causal_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, _dtype_code(q),
                               _ptr(M_in), _ptr(z_in), _ptr(out), M.ctypes.data, z.ctypes.data,
-                              B, H, T, d, dv, float(eps), int(mutation))
+                              B, H, T, d, dv, float(eps), _phi_kind(phi), int(mutation))
     return out, M, z
 
 
-def prefill(q, k, v, M_in=None, z_in=None, eps=1e-6, mutation=0):
+def prefill(q, k, v, M_in=None, z_in=None, eps=1e-6, mutation=0, phi="elu1"):
     """Final state and last-token output. Returns (out_last [B,H,dv], M, z)."""
     q, k, v = _c(q), _c(k), _c(v)
     B, H, T, d = q.shape
@@ -139,11 +153,11 @@ def prefill(q, k, v, M_in=None, z_in=None, eps=1e-6, mutation=0):
     z = np.empty((B, H, d))
     _load().oracle_prefill(q.ctypes.data, k.ctypes.data, v.ctypes.data, _dtype_code(q),
                            _ptr(M_in), _ptr(z_in), out.ctypes.data, M.ctypes.data, z.ctypes.data,
-                           B, H, T, d, dv, float(eps), int(mutation))
+                           B, H, T, d, dv, float(eps), _phi_kind(phi), int(mutation))
     return out, M, z
 
 
-def decode_step(q, k, v, M, z, eps=1e-6, mutation=0):
+def decode_step(q, k, v, M, z, eps=1e-6, mutation=0, phi="elu1"):
     """One recurrent step. q, k: [N,H,d]; v: [N,H,dv]; M [N,H,d,dv], z [N,H,d]
     float64 (not modified). Returns (out [N,H,dv], M_new, z_new)."""
     q, k, v = _c(q), _c(k), _c(v)
@@ -155,7 +169,7 @@ def decode_step(q, k, v, M, z, eps=1e-6, mutation=0):
     out = np.empty((N, H, dv))
     _load().oracle_decode_step(q.ctypes.data, k.ctypes.data, v.ctypes.data, _dtype_code(q),
                                M2.ctypes.data, z2.ctypes.data, out.ctypes.data,
-                               N, H, d, dv, float(eps), int(mutation))
+                               N, H, d, dv, float(eps), _phi_kind(phi), int(mutation))
     return out, M2, z2
 
 
@@ -259,6 +273,40 @@ def noncausal(q, k, v, eps=1e-6):
     M = np.einsum("bhsd,bhsv->bhdv", K, V)
     z = K.sum(2)
     return np.einsum("bhtd,bhdv->bhtv", Q, M) / (np.einsum("bhtd,bhd->bht", Q, z) + eps)[..., None]
+
+
+# ---------------------------------------------------------------------------
+# other feature maps (inputs of the identity path)
+
+def phi_prf(x, W):
+    """Positive random features: phi(x) = exp(W x - |x|^2 / 2) / sqrt(m) for x [..., d] and
+    W [m, d] (storage arrays; float64 arithmetic). The page "Attention_Kernel_Mask" lists
+    positive random features (PRF) and orthogonal random features (ORF) among the feature
+    maps of its non-causal kernel discussion without printing them; this is the positive
+    random-feature map of that family, whose expectation over Gaussian rows w ~ N(0, I_d)
+    gives E[phi(q) . phi(k)] = exp(q . k). The result is a feature vector per token, to be
+    used with phi='identity'."""
+    X = _f64(x)
+    Wf = _f64(W)
+    m = Wf.shape[0]
+    return np.exp(X @ Wf.T - 0.5 * (X * X).sum(-1, keepdims=True)) / np.sqrt(m)
+
+
+def orf_matrix(G, N):
+    """Orthogonal random features from Gaussian draws G and N, both [m, d] with m a multiple
+    of d: every block of d rows of G is orthogonalised (Q of its QR factorisation, a library
+    step), and row i is then scaled to the norm of row i of N, so that each row has the
+    length distribution of a Gaussian row while the rows of a block are exactly
+    orthogonal. Returns W [m, d] float64."""
+    G = np.asarray(G, dtype=np.float64)
+    N = np.asarray(N, dtype=np.float64)
+    m, d = G.shape
+    assert m % d == 0 and N.shape == G.shape
+    W = np.empty((m, d))
+    for b0 in range(0, m, d):
+        Q, _ = np.linalg.qr(G[b0:b0 + d].T)   # columns of Q: orthonormal basis
+        W[b0:b0 + d] = Q.T
+    return W * np.linalg.norm(N, axis=1, keepdims=True)
 
 
 # ---------------------------------------------------------------------------

@@ -21,8 +21,14 @@
  *   which is the segment-wise use described on that page.
  *
  * Inputs are the storage arrays the GPU also reads: bf16 bit patterns
- * (dtype 1) or float32 (dtype 0), contiguous [B, H, T, d] for q and k and
- * [B, H, T, dv] for v. They are widened exactly to float64 before use.
+ * (dtype 1), float32 (dtype 0) or float64 (dtype 2), contiguous [B, H, T, d]
+ * for q and k and [B, H, T, dv] for v. They are widened exactly to float64
+ * before use.
+ *
+ * The feature map: phi_kind 0 is elu(x) + 1 on q and k (the map above);
+ * phi_kind 1 takes q and k as feature values already (phi applied by the
+ * caller, for instance a random-feature map), so that other feature maps run
+ * through the same recurrence.
  *
  * The `mutation` argument exists only so the pin tests can show that each
  * planted mistake is caught; 0 is the oracle proper:
@@ -39,6 +45,7 @@
 #include <string.h>
 
 static inline double widen(const void* base, int dtype, int64_t i) {
+    if (dtype == 2) return ((const double*)base)[i];
     if (dtype == 1) {
         union { uint32_t u; float f; } c;
         c.u = (uint32_t)((const uint16_t*)base)[i] << 16;
@@ -52,19 +59,24 @@ static inline double phi(double x, int mutation) {
     return x > 0.0 ? x + 1.0 : exp(x);
 }
 
+/* The feature map of q and k: elu + 1 (phi_kind 0), or the values as given (phi_kind 1). */
+static inline double phi_qk(double x, int phi_kind, int mutation) {
+    return phi_kind == 1 ? x : phi(x, mutation);
+}
+
 /* One (batch, head) stream: T tokens, state carried in M (d x dv) and z (d).
  * out (T x dv) may be NULL; if last_only, only row T-1 is written to out[0..dv). */
 static void stream_fwd(const void* q, const void* k, const void* v, int dtype,
                        int64_t qoff, int64_t voff, int64_t T, int d, int dv,
                        double eps, double* M, double* z, double* out, int last_only,
-                       int mutation) {
+                       int phi_kind, int mutation) {
     double* fq = (double*)malloc(sizeof(double) * (size_t)d);
     double* fk = (double*)malloc(sizeof(double) * (size_t)d);
     double* vv = (double*)malloc(sizeof(double) * (size_t)dv);
     for (int64_t t = 0; t < T; ++t) {
         for (int i = 0; i < d; ++i) {
-            fq[i] = phi(widen(q, dtype, qoff + t * d + i), mutation);
-            fk[i] = phi(widen(k, dtype, qoff + t * d + i), mutation);
+            fq[i] = phi_qk(widen(q, dtype, qoff + t * d + i), phi_kind, mutation);
+            fk[i] = phi_qk(widen(k, dtype, qoff + t * d + i), phi_kind, mutation);
         }
         for (int j = 0; j < dv; ++j) {
             double x = widen(v, dtype, voff + t * dv + j);
@@ -140,7 +152,7 @@ void oracle_causal_fwd(const void* q, const void* k, const void* v, int dtype,
                        const double* M_in, const double* z_in,
                        double* out, double* M_out, double* z_out,
                        int64_t B, int64_t H, int64_t T, int d, int dv, double eps,
-                       int mutation) {
+                       int phi_kind, int mutation) {
     const int64_t BH = B * H;
     #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t bh = 0; bh < BH; ++bh) {
@@ -148,7 +160,7 @@ void oracle_causal_fwd(const void* q, const void* k, const void* v, int dtype,
         double* z = (double*)malloc(sizeof(double) * (size_t)d);
         load_state(M_in, z_in, bh, d, dv, M, z);
         stream_fwd(q, k, v, dtype, bh * T * d, bh * T * dv, T, d, dv, eps, M, z,
-                   out ? out + bh * T * dv : NULL, 0, mutation);
+                   out ? out + bh * T * dv : NULL, 0, phi_kind, mutation);
         store_state(M_out, z_out, bh, d, dv, M, z);
         free(M);
         free(z);
@@ -161,7 +173,7 @@ void oracle_prefill(const void* q, const void* k, const void* v, int dtype,
                     const double* M_in, const double* z_in,
                     double* out_last, double* M_out, double* z_out,
                     int64_t B, int64_t H, int64_t T, int d, int dv, double eps,
-                    int mutation) {
+                    int phi_kind, int mutation) {
     const int64_t BH = B * H;
     #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t bh = 0; bh < BH; ++bh) {
@@ -169,7 +181,7 @@ void oracle_prefill(const void* q, const void* k, const void* v, int dtype,
         double* z = (double*)malloc(sizeof(double) * (size_t)d);
         load_state(M_in, z_in, bh, d, dv, M, z);
         stream_fwd(q, k, v, dtype, bh * T * d, bh * T * dv, T, d, dv, eps, M, z,
-                   out_last ? out_last + bh * dv : NULL, 1, mutation);
+                   out_last ? out_last + bh * dv : NULL, 1, phi_kind, mutation);
         store_state(M_out, z_out, bh, d, dv, M, z);
         free(M);
         free(z);
@@ -181,12 +193,13 @@ void oracle_prefill(const void* q, const void* k, const void* v, int dtype,
  * [N, H, d], updated in place; out: [N, H, dv] float64. */
 void oracle_decode_step(const void* q, const void* k, const void* v, int dtype,
                         double* M, double* z, double* out,
-                        int64_t N, int64_t H, int d, int dv, double eps, int mutation) {
+                        int64_t N, int64_t H, int d, int dv, double eps, int phi_kind,
+                        int mutation) {
     const int64_t NH = N * H;
     #pragma omp parallel for schedule(static)
     for (int64_t nh = 0; nh < NH; ++nh) {
         stream_fwd(q, k, v, dtype, nh * d, nh * dv, 1, d, dv, eps,
-                   M + nh * (int64_t)d * dv, z + nh * d, out + nh * dv, 0, mutation);
+                   M + nh * (int64_t)d * dv, z + nh * d, out + nh * dv, 0, phi_kind, mutation);
     }
 }
 

@@ -79,6 +79,14 @@ def normal(seed: int, tensor_id: int, shape, scale: float = 1.0, dtype: str = "b
     return out
 
 
+def to_bf16_bits(x) -> np.ndarray:
+    """Round values to float32 and then to bf16 (round to nearest even), as uint16 bit
+    patterns: a storage conversion (finite values only)."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
 def negate(arr: np.ndarray) -> np.ndarray:
     """-x of a storage array, exactly (bf16: the sign bit flipped)."""
     if arr.dtype == np.uint16:

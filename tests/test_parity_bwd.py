@@ -4,6 +4,8 @@ per head as max|diff| / max|ref| over that head's tensor; rows are not normalise
 by one because some cancel to nearly zero by construction (the first token's output
 depends on q only through eps). Tolerances: <= 1e-4 on the float32 path, <= 2e-2 for
 bf16 inputs and gradients (float32 arithmetic inside)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -48,17 +50,22 @@ def bwd(q, k, v, dout, M_in=None, z_in=None, dM_out=None, dz_out=None, eps=1e-6,
     ws = torch.empty(nws, dtype=torch.uint8, device=q.device)
     la.la_causal_bwd_ex(q, k, v, dout, M_in, z_in, dM_out, dz_out, dq, dk, dvv, dM_in, dz_in, B, H, T, d, dv, eps,
                         dtype_code(q), ws, nws)
-    assert la.la_last_launch_count() == 6
+    # bf16 with d, dv in {64, 128}: the tensor-core kernels (chunk sums, scan, dq, reverse scan,
+    # dk and dv); otherwise the float32 SIMT kernels (one more launch)
+    tc = q.dtype == torch.bfloat16 and d in (64, 128) and dv in (64, 128) and not os.environ.get("LA_FORCE_SIMT")
+    assert la.la_last_launch_count() == (5 if tc else 6)
     check_status()
     return dq, dk, dvv, dM_in, dz_in
 
 
-def _compare(got, ref, tol):
+def _compare(got, ref, tol, name=None):
     errs = {}
-    for name, g, r in zip(("dq", "dk", "dv", "dM_in", "dz_in"), got, ref):
+    for key, g, r in zip(("dq", "dk", "dv", "dM_in", "dz_in"), got, ref):
         if g is None:
             continue
-        errs[name] = oracle.rel_err_state(to_host(g), r, tuple(range(2, r.ndim)))
+        errs[key] = oracle.rel_err_state(to_host(g), r, tuple(range(2, r.ndim)))
+    if name:
+        print(f"PARITY bwd_{name} " + " ".join(f"{k}={v:.3e}" for k, v in errs.items()))
     assert max(errs.values()) <= tol, errs
     return errs
 
@@ -94,7 +101,40 @@ def test_fp32_zero_state_and_no_state_gradients():
 @pytest.mark.parametrize("d,dv,T", [(64, 64, 200), (128, 128, 130), (64, 128, 100), (128, 64, 64), (32, 16, 333)])
 def test_bf16_shapes_with_state(d, dv, T):
     got, ref = _case(500 + d + dv + T, 2, 3, T, d, dv, "bf16", 0.5)
-    _compare(got, ref, TOL_BF16)
+    _compare(got, ref, TOL_BF16, f"shapes_d{d}_dv{dv}_T{T}")
+
+
+@pytest.mark.parametrize("T", [1, 63, 65, 129])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_tensor_core_short_and_ragged(d, T):
+    got, ref = _case(540 + d + T, 1, 3, T, d, d, "bf16", 0.5)
+    _compare(got, ref, TOL_BF16, f"ragged_d{d}_T{T}")
+
+
+@pytest.mark.parametrize("case", ["eps", "large"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_tensor_core_edges(case, d):
+    """eps-dominated denominators (q, k ~ -9 + 0.5 N(0,1)) and inputs at scale 4."""
+    B, H, T = 1, 2, 300
+    if case == "eps":
+        q = synthetic.normal(560 + d, 0, (B, H, T, d), 0.5, "bf16", shift=-9.0)
+        k = synthetic.normal(560 + d, 1, (B, H, T, d), 0.5, "bf16", shift=-9.0)
+        v = synthetic.normal(560 + d, 2, (B, H, T, d), 0.5, "bf16")
+    else:
+        q, k, v = (synthetic.normal(560 + d, i, (B, H, T, d), 4.0, "bf16") for i in range(3))
+    dout = synthetic.normal(560 + d, 7, (B, H, T, d), 1.0, "bf16")
+    ref = oracle.causal_bwd(q, k, v, _values(dout))
+    got = bwd(to_dev(q), to_dev(k), to_dev(v), to_dev(dout))
+    _compare(got, ref, TOL_BF16, f"{case}_d{d}")
+
+
+def test_bf16_tensor_core_and_simt_paths_agree(monkeypatch):
+    got_tc, ref = _case(580, 1, 2, 400, 128, 128, "bf16", 0.5)
+    monkeypatch.setenv("LA_FORCE_SIMT", "1")
+    got_simt, _ = _case(580, 1, 2, 400, 128, 128, "bf16", 0.5)
+    for a, b in zip(got_tc, got_simt):
+        r = to_host(b)
+        assert np.abs(to_host(a) - r).max() <= TOL_BF16 * np.abs(r).max()
 
 
 def test_bf16_training_workload_sampled_heads():
@@ -108,7 +148,7 @@ def test_bf16_training_workload_sampled_heads():
         sl = lambda a: np.ascontiguousarray(a[b:b + 1, h:h + 1])
         ref = oracle.causal_bwd(sl(q), sl(k), sl(v), _values(sl(dout)))
         head = [g[b:b + 1, h:h + 1] for g in got]
-        _compare(head, ref, TOL_BF16)
+        _compare(head, ref, TOL_BF16, f"workload_train_b{b}h{h}")
 
 
 def test_bf16_segment_call_shape_sampled_heads():
@@ -122,7 +162,7 @@ def test_bf16_segment_call_shape_sampled_heads():
     for b, h in ((0, 0), (1, 17), (1, 31)):
         sl = lambda a: np.ascontiguousarray(a[b:b + 1, h:h + 1])
         ref = oracle.causal_bwd(sl(q), sl(k), sl(v), _values(sl(dout)), sl(M0), sl(z0), sl(dM), sl(dz))
-        _compare([g[b:b + 1, h:h + 1] for g in got], ref, TOL_BF16)
+        _compare([g[b:b + 1, h:h + 1] for g in got], ref, TOL_BF16, f"segment_shape_b{b}h{h}")
 
 
 # ------------------------------------------------------------------ properties and the ABI
