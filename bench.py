@@ -524,11 +524,12 @@ def run_modes(dev):
     flops = 2 * B * H * nch * (5 * C * d * dv + C * (C + 1) // 2 * (3 * d + 4 * dv))
     res["train_bwd"] = {"workload": f"B={B} H={H} T={T} d=dv={d} bf16, dout ~ N(0,1), dq, dk, dv + dM_in, dz_in",
                         "value": round(B * T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(ms, 5),
-                        "launches": 6,
+                        "launches": la.la_last_launch_count(),
+                        "kernels": "tensor-core chunk kernels (chunk sums, scan, dq, reverse scan, dk/dv)",
                         "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
                                      "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                      "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs",
-                                     "fp32_simt_tflops": round(flops / (ms / 1e3) / 1e12, 2)}}
+                                     "product_tflops": round(flops / (ms / 1e3) / 1e12, 2)}}
     del q, k, v, out, ws, dout, dq, dk, dvv
 
     w = synthetic.WORKLOADS["generation"]

@@ -530,19 +530,22 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
     const bool bf16 = dtype == LA_BF16;
 
     const bool tc = bf16 && (d == 64 || d == 128) && (dv_dim == 64 || dv_dim == 128) &&
-                    env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31);
+                    env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31) && aligned16(dq) &&
+                    aligned16(dk) && aligned16(dv);  // the gradients are stored in 16-byte vectors
     if (tc) {
         // tensor-core chunk kernels: per-chunk key-value sums (parts_tc with 64-token parts),
         // the prefix scan, dq (with g, e and the chunk sums of the state gradient), the
         // reverse scan, then dk and dv
         const Strides st = contiguous(H, T, d, dv_dim);
-        CUtensorMap mq, mk, mv, mdo, mg;
+        CUtensorMap mq, mk, mv, mdo, mg, mgl;
         void* G = wsf + off_G;
+        void* Glo = static_cast<__nv_bfloat16*>(G) + BH * T * dv_dim;  // low parts after the high parts
         if (!make_map(&mq, q, d, T, H, B, st.q_st, st.q_sh, st.q_sb) ||
             !make_map(&mk, k, d, T, H, B, st.k_st, st.k_sh, st.k_sb) ||
             !make_map(&mv, v, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
             !make_map(&mdo, dout, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
-            !make_map(&mg, G, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb))
+            !make_map(&mg, G, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
+            !make_map(&mgl, Glo, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb))
             return LA_ERR_CUDA;
         PartsParams pp{};
         pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv_dim, pp.rec_M = rec, pp.rec_z = rec;
@@ -566,7 +569,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
         rp.BH = (int)BH, rp.nch = (int)nch, rp.d = d, rp.dv = dv_dim, rp.len = rec, rp.reverse = true;
         if ((rc = cuda_rc(launch_scan_states(rp, stream)))) return rc;
         ++t_launches;
-        if ((rc = cuda_rc(launch_bwd_dkdv_tc(tp, mq, mk, mv, mg, stream)))) return rc;
+        if ((rc = cuda_rc(launch_bwd_dkdv_tc(tp, mq, mk, mv, mg, mgl, stream)))) return rc;
         ++t_launches;
         return LA_OK;
     }

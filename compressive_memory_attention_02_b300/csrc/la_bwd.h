@@ -46,8 +46,8 @@ struct ScanParams {
 // Tensor-core chunk kernels (la_bwd_tc.cu), bf16 storage, d and dv in {64, 128}: one block
 // per (64-token chunk, b*H + h). states / rev: the records above (the state before each
 // chunk; the chunk sums phi(Q)^T G and phi(Q)^T e, then after the reverse scan the state
-// gradient from every token after the chunk); G: g_t as bf16 [B*H][T][dv] (in the G
-// region); E: e_t.
+// gradient from every token after the chunk); G: g_t as bf16 high parts [B*H][T][dv] and,
+// right after them, the bf16 remainders (both in the G region, sized for f32); E: e_t.
 struct BwdTcParams {
     void* dq;
     void* dk;
@@ -67,7 +67,8 @@ struct BwdTcParams {
 cudaError_t launch_bwd_dq_tc(const BwdTcParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_tc(const BwdTcParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                               const CUtensorMap& mv, const CUtensorMap& mg, cudaStream_t s);
+                               const CUtensorMap& mv, const CUtensorMap& mg, const CUtensorMap& mgl,
+                               cudaStream_t s);
 
 size_t bwd_workspace_floats(int64_t BH, int64_t T, int d, int dv, size_t* off_rev, size_t* off_G, size_t* off_E);
 cudaError_t launch_scan_states(const ScanParams& p, cudaStream_t s);

@@ -19,6 +19,11 @@
 // la_bwd.cu over per-chunk records; G (bf16) and e (f32) pass from the first kernel to
 // the second through the workspace.
 //
+// G, P and dA are formed in f32 inside the kernels; each enters its products as two bf16
+// operands, a high part and the rounded remainder (x = hi + lo to ~16 bits), so that the
+// cancellations in dq (M g + e z against the intra-chunk sum, and g . v_j + e inside dA)
+// act on f32-accurate values; the other operands (phi, V, dout, the states) are bf16.
+//
 // Each block runs its steps in sequence (load, phi, MMAs, element-wise passes), with
 // several blocks per SM overlapping each other. 256 threads: warp w may touch only TMEM
 // lane quarter w % 4; per-token passes use warps 0 and 1 (lanes 0-63 = the chunk's
@@ -29,7 +34,9 @@
 // features] per atom as TMA loads them (the dq kernel's K tile has 80 rows per atom: row
 // 64 holds bf16 z, rows 65-79 zero); the state tile (M or R, bf16) [d rows][64 dv] per
 // block of d * 128 bytes, read MN-major (K = d) and K-major (K = dv); P, dA and their
-// transposes [64][64] K-major.
+// transposes [64][64] K-major; the high and low parts of G, P and dA in adjacent tiles.
+// Every A-operand tile of 64 rows is followed by at least one atom of shared memory (an
+// M = 128 MMA reads 64 rows past it; those rows of the result are never used).
 #include "la_bwd.h"
 #include "la_tc_common.cuh"
 
@@ -50,6 +57,12 @@ __device__ __forceinline__ void state_to_tile(const float* rec, uint8_t* tile, i
         const uint4 w = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
         *reinterpret_cast<uint4*>(tile + (j0 >> 6) * (D * 128) + i * 128 + ((((j0 & 63) >> 3) ^ (i & 7)) << 4)) = w;
     }
+}
+
+// Two f32 values as bf16 high parts (hi) and bf16 remainders (lo): x = hi + lo to ~16 bits.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16(a, b);
+    lo = pack_bf16(a - bf16lo(hi), b - bf16hi(hi));
 }
 
 // bf16 element (row, col) of a tile with 64-column atoms `astride` bytes apart
@@ -87,11 +100,11 @@ struct DqLayout {
     static constexpr int KT = QT + D / 64 * ATOM;         // [phi(K); z], D/64 atoms of 80 rows
     static constexpr int VT = KT + D / 64 * ATOMK;        // V, DV/64 atoms
     static constexpr int OT = VT + DV / 64 * ATOM;        // dout, DV/64 atoms
-    static constexpr int MT = OT + DV / 64 * ATOM;        // state M (bf16), DV/64 blocks of D*128 bytes
-    static constexpr int PT = MT + D * DV * 2;            // P [64][64] + one atom read past by M = 128
-    static constexpr int GT = PT + 2 * ATOM;              // G, DV/64 atoms + one read past
-    static constexpr int AT = GT + (DV / 64 + 1) * ATOM;  // dA [64][64] + one read past
-    static constexpr int DEN = AT + 2 * ATOM;             // 64 floats: D_t
+    static constexpr int PT = OT + DV / 64 * ATOM;        // P high, then low part [64][64]
+    static constexpr int GT = PT + 2 * ATOM;              // G high (DV/64 atoms), then low part
+    static constexpr int AT = GT + 2 * (DV / 64) * ATOM;  // dA high, then low part
+    static constexpr int MT = AT + 2 * ATOM;              // state M (bf16), DV/64 blocks of D*128 bytes
+    static constexpr int DEN = MT + D * DV * 2;           // 64 floats: D_t
     static constexpr int EV = DEN + 256;                  // 64 floats: e_t
     static constexpr int ZF = EV + 256;                   // D floats: z
     static constexpr int BAR = ZF + 512;
@@ -223,17 +236,20 @@ __global__ void __launch_bounds__(BT, 1)
         for (int k0 = 0; k0 < 64; k0 += 16) {
             float x[16];
             ld16f(srow + k0, x);
-            uint32_t pk[8];
+            uint32_t ph[8], pl[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float s0 = (k0 + 2 * e <= t) ? x[2 * e] : 0.f;
                 const float s1 = (k0 + 2 * e + 1 <= t) ? x[2 * e + 1] : 0.f;
-                pk[e] = pack_bf16(s0, s1);
+                split2(s0, s1, ph[e], pl[e]);
                 rs += s0 + s1;
             }
             const int ch = k0 >> 3;  // 16-byte chunks ch, ch + 1 of the row
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4*>(prow + (((ch + 1) ^ (t & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            const uint32_t c0 = (ch ^ (t & 7)) << 4, c1 = ((ch + 1) ^ (t & 7)) << 4;
+            *reinterpret_cast<uint4*>(prow + c0) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+            *reinterpret_cast<uint4*>(prow + c1) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+            *reinterpret_cast<uint4*>(prow + ATOM + c0) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            *reinterpret_cast<uint4*>(prow + ATOM + c1) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
         }
         const float zq = __uint_as_float(tmem_ld1(srow + 64));
         tmem_wait_ld();
@@ -247,8 +263,10 @@ __global__ void __launch_bounds__(BT, 1)
     if (ok && tid == 0) {
         constexpr uint32_t id_pv = idesc_bf16(128, DV, 0, 1);
 #pragma unroll
-        for (int ks = 0; ks < CH / 16; ++ks)
+        for (int ks = 0; ks < CH / 16; ++ks) {
             mma_bf16_ss(tmem + L::TO, dPk + off(ks * 32), dVm + off(ks * 2048), id_pv, 1);
+            mma_bf16_ss(tmem + L::TO, dPk + off(ATOM + ks * 32), dVm + off(ks * 2048), id_pv, 1);
+        }
         mma_commit(mma_done);
     }
     ok = ok && block_wait(mma_done, phase++ & 1, abort_flag, p.status);
@@ -259,27 +277,35 @@ __global__ void __launch_bounds__(BT, 1)
         const uint32_t orow = tmem + L::TO + ((uint32_t)(32 * warp) << 16);
         const float rd = t < valid ? 1.f / den[t] : 0.f;  // rows past the end: g = e = 0
         float dot = 0.f;
+        // workspace: the high parts of G as [B*H][T][dv] bf16, the low parts right after them
         __nv_bfloat16* gout = reinterpret_cast<__nv_bfloat16*>(p.G) + ((int64_t)bh * p.T + t0 + t) * DV;
+        const int64_t glo = (int64_t)p.B * p.H * p.T * DV;
 #pragma unroll 1
         for (int j0 = 0; j0 < DV; j0 += 16) {
             float o[16];
             ld16f(orow + j0, o);
-            uint32_t gk[8];
+            uint32_t gh[8], gl[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint32_t dw = *reinterpret_cast<const uint32_t*>(sm + L::OT + tile_off(t, j0 + 2 * e, ATOM));
                 const float g0 = bf16lo(dw) * rd, g1 = bf16hi(dw) * rd;
                 dot += g0 * o[2 * e] + g1 * o[2 * e + 1];
-                gk[e] = pack_bf16(g0, g1);
+                split2(g0, g1, gh[e], gl[e]);
             }
             uint8_t* grow = sm + L::GT + (j0 >> 6) * ATOM + t * 128;
             const int ch = (j0 & 63) >> 3;
-            const uint4 lo = make_uint4(gk[0], gk[1], gk[2], gk[3]), hi = make_uint4(gk[4], gk[5], gk[6], gk[7]);
-            *reinterpret_cast<uint4*>(grow + ((ch ^ (t & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(grow + (((ch + 1) ^ (t & 7)) << 4)) = hi;
+            const uint32_t c0 = (ch ^ (t & 7)) << 4, c1 = ((ch + 1) ^ (t & 7)) << 4;
+            const uint4 h0 = make_uint4(gh[0], gh[1], gh[2], gh[3]), h1 = make_uint4(gh[4], gh[5], gh[6], gh[7]);
+            const uint4 l0 = make_uint4(gl[0], gl[1], gl[2], gl[3]), l1 = make_uint4(gl[4], gl[5], gl[6], gl[7]);
+            *reinterpret_cast<uint4*>(grow + c0) = h0;
+            *reinterpret_cast<uint4*>(grow + c1) = h1;
+            *reinterpret_cast<uint4*>(grow + (DV / 64) * ATOM + c0) = l0;
+            *reinterpret_cast<uint4*>(grow + (DV / 64) * ATOM + c1) = l1;
             if (t < valid) {
-                *reinterpret_cast<uint4*>(gout + j0) = lo;
-                *reinterpret_cast<uint4*>(gout + j0 + 8) = hi;
+                *reinterpret_cast<uint4*>(gout + j0) = h0;
+                *reinterpret_cast<uint4*>(gout + j0 + 8) = h1;
+                *reinterpret_cast<uint4*>(gout + glo + j0) = l0;
+                *reinterpret_cast<uint4*>(gout + glo + j0 + 8) = l1;
             }
         }
         const float e = -dot * rd;  // g . out = (g . O) / D
@@ -295,16 +321,21 @@ __global__ void __launch_bounds__(BT, 1)
         constexpr uint32_t id_a = idesc_bf16(128, CH, 0, 0);
         constexpr uint32_t id_q = idesc_bf16(128, D, 0, 0);
         constexpr uint32_t id_r = idesc_bf16(128, DV, 1, 1);
+        constexpr uint32_t GLO = (DV / 64) * ATOM;  // offset of the low parts of G
 #pragma unroll
         for (int ks = 0; ks < DV / 16; ++ks) {
             const uint32_t go = (ks >> 2) * ATOM + (ks & 3) * 32;
+            const uint64_t mo = off((ks >> 2) * (D * 128) + (ks & 3) * 32);
             mma_bf16_ss(tmem + L::TS, dGk + off(go), dVk + off(go), id_a, ks != 0);
-            mma_bf16_ss(tmem + L::TO, dGk + off(go), dMk + off((ks >> 2) * (D * 128) + (ks & 3) * 32), id_q,
-                        ks != 0);
+            mma_bf16_ss(tmem + L::TS, dGk + off(GLO + go), dVk + off(go), id_a, 1);
+            mma_bf16_ss(tmem + L::TO, dGk + off(go), dMk + mo, id_q, ks != 0);
+            mma_bf16_ss(tmem + L::TO, dGk + off(GLO + go), dMk + mo, id_q, 1);
         }
 #pragma unroll
-        for (int ks = 0; ks < CH / 16; ++ks)
+        for (int ks = 0; ks < CH / 16; ++ks) {
             mma_bf16_ss(tmem + L::TR, dQm + off(ks * 2048), dGm + off(ks * 2048), id_r, ks != 0);
+            mma_bf16_ss(tmem + L::TR, dQm + off(ks * 2048), dGm + off(GLO + ks * 2048), id_r, 1);
+        }
         mma_commit(mma_done);
     }
     ok = ok && block_wait(mma_done, phase++ & 1, abort_flag, p.status);
@@ -319,16 +350,19 @@ __global__ void __launch_bounds__(BT, 1)
         for (int k0 = 0; k0 < 64; k0 += 16) {
             float x[16];
             ld16f(arow + k0, x);
-            uint32_t pk[8];
+            uint32_t ah[8], al[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float a0 = (k0 + 2 * q <= t) ? x[2 * q] + e : 0.f;
                 const float a1 = (k0 + 2 * q + 1 <= t) ? x[2 * q + 1] + e : 0.f;
-                pk[q] = pack_bf16(a0, a1);
+                split2(a0, a1, ah[q], al[q]);
             }
             const int ch = k0 >> 3;
-            *reinterpret_cast<uint4*>(row + ((ch ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4*>(row + (((ch + 1) ^ (t & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            const uint32_t c0 = (ch ^ (t & 7)) << 4, c1 = ((ch + 1) ^ (t & 7)) << 4;
+            *reinterpret_cast<uint4*>(row + c0) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+            *reinterpret_cast<uint4*>(row + c1) = make_uint4(ah[4], ah[5], ah[6], ah[7]);
+            *reinterpret_cast<uint4*>(row + ATOM + c0) = make_uint4(al[0], al[1], al[2], al[3]);
+            *reinterpret_cast<uint4*>(row + ATOM + c1) = make_uint4(al[4], al[5], al[6], al[7]);
         }
         fence_proxy_async_smem();
     }
@@ -362,8 +396,10 @@ __global__ void __launch_bounds__(BT, 1)
     if (ok && tid == 0) {
         constexpr uint32_t id_q = idesc_bf16(128, D, 0, 1);
 #pragma unroll
-        for (int ks = 0; ks < CH / 16; ++ks)
+        for (int ks = 0; ks < CH / 16; ++ks) {
             mma_bf16_ss(tmem + L::TO, dAk + off(ks * 32), dKm + off(ks * 2048), id_q, 1);
+            mma_bf16_ss(tmem + L::TO, dAk + off(ATOM + ks * 32), dKm + off(ks * 2048), id_q, 1);
+        }
         mma_commit(mma_done);
     }
     ok = ok && block_wait(mma_done, phase++ & 1, abort_flag, p.status);
@@ -408,11 +444,11 @@ struct DkvLayout {
     static constexpr int QT = 0;                          // phi(Q), D/64 atoms
     static constexpr int KT = QT + D / 64 * ATOM;         // phi(K), D/64 atoms (+ read past: VT)
     static constexpr int VT = KT + D / 64 * ATOM;         // V, DV/64 atoms (+ read past: GT)
-    static constexpr int GT = VT + DV / 64 * ATOM;        // G, DV/64 atoms
-    static constexpr int RT = GT + DV / 64 * ATOM;        // R (bf16), DV/64 blocks of D*128 bytes
-    static constexpr int PT = RT + D * DV * 2;            // P^T [64 keys][64 queries] + read past
-    static constexpr int AT = PT + 2 * ATOM;              // dA^T + read past
-    static constexpr int EV = AT + 2 * ATOM;              // 64 floats: e_t
+    static constexpr int GT = VT + DV / 64 * ATOM;        // G high (DV/64 atoms), then low part
+    static constexpr int PT = GT + 2 * (DV / 64) * ATOM;  // P^T [64 keys][64 queries] high, then low
+    static constexpr int AT = PT + 2 * ATOM;              // dA^T high, then low
+    static constexpr int RT = AT + 2 * ATOM;              // R (bf16), DV/64 blocks of D*128 bytes
+    static constexpr int EV = RT + D * DV * 2;            // 64 floats: e_t
     static constexpr int RV = EV + 256;                   // D floats: r
     static constexpr int BAR = RV + 512;
     static constexpr int MISC = BAR + 16;
@@ -428,7 +464,7 @@ template <int D, int DV>
 __global__ void __launch_bounds__(BT, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
-                       BwdTcParams p) {
+                       const __grid_constant__ CUtensorMap mgl, BwdTcParams p) {
     using L = DkvLayout<D, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
@@ -456,6 +492,7 @@ __global__ void __launch_bounds__(BT, 1)
         tma_prefetch_desc(&mk);
         tma_prefetch_desc(&mv);
         tma_prefetch_desc(&mg);
+        tma_prefetch_desc(&mgl);
     }
     if (warp == 0) {
         tmem_alloc(tmem_holder, L::NCOL);
@@ -468,7 +505,7 @@ __global__ void __launch_bounds__(BT, 1)
 
     if (tid == 0) {
         const uint64_t pol = l2_evict_first_policy();
-        mbar_expect_tx(ld_full, (2 * D + 2 * DV) * CH * 2);
+        mbar_expect_tx(ld_full, (2 * D + 3 * DV) * CH * 2);
         for (int a = 0; a < D / 64; ++a) {
             tma_load_4d_hint(sm + L::QT + a * ATOM, &mq, ld_full, a * 64, (int)t0, h, b, pol);
             tma_load_4d_hint(sm + L::KT + a * ATOM, &mk, ld_full, a * 64, (int)t0, h, b, pol);
@@ -476,6 +513,7 @@ __global__ void __launch_bounds__(BT, 1)
         for (int a = 0; a < DV / 64; ++a) {
             tma_load_4d_hint(sm + L::VT + a * ATOM, &mv, ld_full, a * 64, (int)t0, h, b, pol);
             tma_load_4d_hint(sm + L::GT + a * ATOM, &mg, ld_full, a * 64, (int)t0, h, b, pol);
+            tma_load_4d_hint(sm + L::GT + (DV / 64 + a) * ATOM, &mgl, ld_full, a * 64, (int)t0, h, b, pol);
         }
     }
     state_to_tile<D, DV>(rrec, sm + L::RT, tid);
@@ -516,6 +554,7 @@ __global__ void __launch_bounds__(BT, 1)
         for (int ks = 0; ks < DV / 16; ++ks) {
             const uint32_t o = (ks >> 2) * ATOM + (ks & 3) * 32;
             mma_bf16_ss(tmem + L::TA, dVk + off(o), dGk + off(o), id_t, ks != 0);
+            mma_bf16_ss(tmem + L::TA, dVk + off(o), dGk + off((DV / 64) * ATOM + o), id_t, 1);
         }
         mma_commit(mma_done);
     }
@@ -532,19 +571,24 @@ __global__ void __launch_bounds__(BT, 1)
             float s[16], a[16];
             ld16f(tmem + L::TS + lb + k0, s);
             ld16f(tmem + L::TA + lb + k0, a);
-            uint32_t ps[8], pa[8];
+            uint32_t ph[8], pl[8], ah[8], al[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int tq = k0 + 2 * q;
                 const bool m0 = tq >= j, m1 = tq + 1 >= j;
-                ps[q] = pack_bf16(m0 ? s[2 * q] : 0.f, m1 ? s[2 * q + 1] : 0.f);
-                pa[q] = pack_bf16(m0 ? a[2 * q] + ev[tq] : 0.f, m1 ? a[2 * q + 1] + ev[tq + 1] : 0.f);
+                split2(m0 ? s[2 * q] : 0.f, m1 ? s[2 * q + 1] : 0.f, ph[q], pl[q]);
+                split2(m0 ? a[2 * q] + ev[tq] : 0.f, m1 ? a[2 * q + 1] + ev[tq + 1] : 0.f, ah[q], al[q]);
             }
             const int ch = k0 >> 3;
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (j & 7)) << 4)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
-            *reinterpret_cast<uint4*>(prow + (((ch + 1) ^ (j & 7)) << 4)) = make_uint4(ps[4], ps[5], ps[6], ps[7]);
-            *reinterpret_cast<uint4*>(arow + ((ch ^ (j & 7)) << 4)) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-            *reinterpret_cast<uint4*>(arow + (((ch + 1) ^ (j & 7)) << 4)) = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+            const uint32_t c0 = (ch ^ (j & 7)) << 4, c1 = ((ch + 1) ^ (j & 7)) << 4;
+            *reinterpret_cast<uint4*>(prow + c0) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+            *reinterpret_cast<uint4*>(prow + c1) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+            *reinterpret_cast<uint4*>(prow + ATOM + c0) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            *reinterpret_cast<uint4*>(prow + ATOM + c1) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+            *reinterpret_cast<uint4*>(arow + c0) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+            *reinterpret_cast<uint4*>(arow + c1) = make_uint4(ah[4], ah[5], ah[6], ah[7]);
+            *reinterpret_cast<uint4*>(arow + ATOM + c0) = make_uint4(al[0], al[1], al[2], al[3]);
+            *reinterpret_cast<uint4*>(arow + ATOM + c1) = make_uint4(al[4], al[5], al[6], al[7]);
         }
         fence_proxy_async_smem();
     }
@@ -556,10 +600,15 @@ __global__ void __launch_bounds__(BT, 1)
         constexpr uint32_t id_vg = idesc_bf16(128, DV, 0, 1);
         constexpr uint32_t id_kq = idesc_bf16(128, D, 0, 1);
         constexpr uint32_t id_kr = idesc_bf16(128, D, 0, 0);
+        constexpr uint32_t GLO = (DV / 64) * ATOM;
 #pragma unroll
         for (int ks = 0; ks < CH / 16; ++ks) {
+            // P^T G with both split: hi.hi + lo.hi + hi.lo
             mma_bf16_ss(tmem + L::TV, dPk + off(ks * 32), dGm + off(ks * 2048), id_vg, ks != 0);
+            mma_bf16_ss(tmem + L::TV, dPk + off(ATOM + ks * 32), dGm + off(ks * 2048), id_vg, 1);
+            mma_bf16_ss(tmem + L::TV, dPk + off(ks * 32), dGm + off(GLO + ks * 2048), id_vg, 1);
             mma_bf16_ss(tmem + L::TK, dAk + off(ks * 32), dQm + off(ks * 2048), id_kq, ks != 0);
+            mma_bf16_ss(tmem + L::TK, dAk + off(ATOM + ks * 32), dQm + off(ks * 2048), id_kq, 1);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
@@ -637,13 +686,14 @@ static cudaError_t launch_dq_t(const BwdTcParams& p, const CUtensorMap& mq, cons
 
 template <int D, int DV>
 static cudaError_t launch_dkdv_t(const BwdTcParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                                 const CUtensorMap& mv, const CUtensorMap& mg, cudaStream_t s) {
+                                 const CUtensorMap& mv, const CUtensorMap& mg, const CUtensorMap& mgl,
+                                 cudaStream_t s) {
     using L = DkvLayout<D, DV>;
     static_assert(L::ALLOC <= 227 * 1024, "shared memory budget");
     auto fn = bwd_dkdv_tc_kernel<D, DV>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    fn<<<dim3(p.nch, p.B * p.H), BT, L::ALLOC, s>>>(mq, mk, mv, mg, p);
+    fn<<<dim3(p.nch, p.B * p.H), BT, L::ALLOC, s>>>(mq, mk, mv, mg, mgl, p);
     return cudaGetLastError();
 }
 
@@ -657,11 +707,12 @@ cudaError_t launch_bwd_dq_tc(const BwdTcParams& p, const CUtensorMap& mq, const 
 }
 
 cudaError_t launch_bwd_dkdv_tc(const BwdTcParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                               const CUtensorMap& mv, const CUtensorMap& mg, cudaStream_t s) {
-    if (p.d == 128 && p.dv_dim == 128) return launch_dkdv_t<128, 128>(p, mq, mk, mv, mg, s);
-    if (p.d == 128 && p.dv_dim == 64) return launch_dkdv_t<128, 64>(p, mq, mk, mv, mg, s);
-    if (p.d == 64 && p.dv_dim == 128) return launch_dkdv_t<64, 128>(p, mq, mk, mv, mg, s);
-    if (p.d == 64 && p.dv_dim == 64) return launch_dkdv_t<64, 64>(p, mq, mk, mv, mg, s);
+                               const CUtensorMap& mv, const CUtensorMap& mg, const CUtensorMap& mgl,
+                               cudaStream_t s) {
+    if (p.d == 128 && p.dv_dim == 128) return launch_dkdv_t<128, 128>(p, mq, mk, mv, mg, mgl, s);
+    if (p.d == 128 && p.dv_dim == 64) return launch_dkdv_t<128, 64>(p, mq, mk, mv, mg, mgl, s);
+    if (p.d == 64 && p.dv_dim == 128) return launch_dkdv_t<64, 128>(p, mq, mk, mv, mg, mgl, s);
+    if (p.d == 64 && p.dv_dim == 64) return launch_dkdv_t<64, 64>(p, mq, mk, mv, mg, mgl, s);
     return cudaErrorInvalidValue;
 }
 
