@@ -533,43 +533,57 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
                     env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31) && aligned16(dq) &&
                     aligned16(dk) && aligned16(dv);  // the gradients are stored in 16-byte vectors
     if (tc) {
-        // tensor-core chunk kernels: per-chunk key-value sums (parts_tc with 64-token parts),
-        // the prefix scan, dq (with g, e and the chunk sums of the state gradient), the
-        // reverse scan, then dk and dv
+        // tensor-core sweeps over ranges of 64-token chunks: the key-value sum of every range
+        // (parts_tc), the prefix scan over ranges, the dq sweep (with D_t, e_t and each
+        // range's sums of the state gradient), the reverse scan, then the dk/dv sweep
         const Strides st = contiguous(H, T, d, dv_dim);
-        CUtensorMap mq, mk, mv, mdo, mg, mgl;
-        void* G = wsf + off_G;
-        void* Glo = static_cast<__nv_bfloat16*>(G) + BH * T * dv_dim;  // low parts after the high parts
+        CUtensorMap mq, mk, mv, mdo;
         if (!make_map(&mq, q, d, T, H, B, st.q_st, st.q_sh, st.q_sb) ||
             !make_map(&mk, k, d, T, H, B, st.k_st, st.k_sh, st.k_sb) ||
             !make_map(&mv, v, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
-            !make_map(&mdo, dout, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
-            !make_map(&mg, G, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb) ||
-            !make_map(&mgl, Glo, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb))
+            !make_map(&mdo, dout, dv_dim, T, H, B, st.v_st, st.v_sh, st.v_sb))
             return LA_ERR_CUDA;
+        // ranges: the fewest waves of blocks x chunks per block (plus one chunk's worth of
+        // setup per block), ties to longer ranges
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t slots = (int64_t)sms * bwd_sweep_occupancy(d, dv_dim);
+        int64_t cpr = nch, best = -1;
+        const int64_t forced = env_int("LA_BWD_CPR", 0);
+        if (forced > 0) {
+            cpr = forced < nch ? forced : nch;
+        } else {
+            for (int64_t c = nch; c >= 1; --c) {
+                const int64_t nr_c = ceil_div(nch, c);
+                const int64_t cost = ceil_div(BH * nr_c, slots) * (c + 1);
+                if (best < 0 || cost < best) best = cost, cpr = c;
+            }
+        }
+        const int64_t nr = ceil_div(nch, cpr);
         PartsParams pp{};
         pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv_dim, pp.rec_M = rec, pp.rec_z = rec;
-        pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv_dim, pp.part_len = BWD_CH, pp.nparts = (int)nch;
+        pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv_dim, pp.part_len = cpr * BWD_CH, pp.nparts = (int)nr;
         pp.eps = eps, pp.st = st, pp.status = ds->status;
         if ((rc = cuda_rc(launch_parts_tc(pp, mk, mv, stream)))) return rc;
         ++t_launches;
         ScanParams sp{};
-        sp.rec = wsf, sp.base_M = M_in, sp.base_z = z_in, sp.BH = (int)BH, sp.nch = (int)nch;
+        sp.rec = wsf, sp.base_M = M_in, sp.base_z = z_in, sp.BH = (int)BH, sp.nch = (int)nr;
         sp.d = d, sp.dv = dv_dim, sp.len = rec, sp.reverse = false;
         if ((rc = cuda_rc(launch_scan_states(sp, stream)))) return rc;
         ++t_launches;
         BwdTcParams tp{};
-        tp.dq = dq, tp.dk = dk, tp.dv = dv, tp.states = wsf, tp.rev = wsf + off_rev, tp.G = G, tp.E = wsf + off_E;
-        tp.B = B, tp.H = H, tp.T = T, tp.d = d, tp.dv_dim = dv_dim, tp.nch = (int)nch, tp.rec = rec, tp.eps = eps;
-        tp.status = ds->status;
+        tp.dq = dq, tp.dk = dk, tp.dv = dv, tp.states = wsf, tp.rev = wsf + off_rev;
+        tp.Dn = wsf + off_G, tp.E = wsf + off_E;  // D_t in the (here unused) G region
+        tp.B = B, tp.H = H, tp.T = T, tp.d = d, tp.dv_dim = dv_dim, tp.nch = (int)nch;
+        tp.nr = (int)nr, tp.cpr = (int)cpr, tp.rec = rec, tp.eps = eps, tp.status = ds->status;
         if ((rc = cuda_rc(launch_bwd_dq_tc(tp, mq, mk, mv, mdo, stream)))) return rc;
         ++t_launches;
         ScanParams rp{};
         rp.rec = wsf + off_rev, rp.base_M = dM_out, rp.base_z = dz_out, rp.total_M = dM_in, rp.total_z = dz_in;
-        rp.BH = (int)BH, rp.nch = (int)nch, rp.d = d, rp.dv = dv_dim, rp.len = rec, rp.reverse = true;
+        rp.BH = (int)BH, rp.nch = (int)nr, rp.d = d, rp.dv = dv_dim, rp.len = rec, rp.reverse = true;
         if ((rc = cuda_rc(launch_scan_states(rp, stream)))) return rc;
         ++t_launches;
-        if ((rc = cuda_rc(launch_bwd_dkdv_tc(tp, mq, mk, mv, mg, mgl, stream)))) return rc;
+        if ((rc = cuda_rc(launch_bwd_dkdv_tc(tp, mq, mk, mv, mdo, stream)))) return rc;
         ++t_launches;
         return LA_OK;
     }

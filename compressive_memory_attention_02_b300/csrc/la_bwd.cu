@@ -435,42 +435,42 @@ __global__ void __launch_bounds__(NT) bwd_dv_kernel(BwdParams p) {
 }
 
 // ------------------------------------------------------------------ exclusive scans over chunks
-// grid (ceil(len / NT), B*H); thread e walks element e of every record of its bh in chunk
+// grid (ceil(len / 4 / NT), B*H); thread e walks elements 4e..4e+3 of every record of its bh in chunk
 // order (reverse order when asked), replacing each record by the running sum before it.
 __global__ void __launch_bounds__(NT) scan_states_kernel(ScanParams p) {
-    const int64_t e = (int64_t)blockIdx.x * NT + threadIdx.x;
-    if (e >= p.len) return;
+    // four consecutive elements per thread (len = d (dv + 1) and d * dv are multiples of 8,
+    // so a group never straddles M and z and the records' float4 slots are aligned); the
+    // loads of up to G records are issued together, then the exclusive sums are stored
+    constexpr int G = 8;
+    const int64_t n4 = p.len / 4;
+    const int64_t e4 = (int64_t)blockIdx.x * NT + threadIdx.x;
+    if (e4 >= n4) return;
     const int bh = blockIdx.y;
-    const int64_t dd = (int64_t)p.d * p.dv;
-    float run = 0.f;
-    if (e < dd) {
-        if (p.base_M) run = p.base_M[(int64_t)bh * dd + e];
-    } else if (p.base_z) {
-        run = p.base_z[(int64_t)bh * p.d + (e - dd)];
-    }
-    float* r = p.rec + (int64_t)bh * p.nch * p.len + e;
-    auto at = [&](int i) -> float& { return r[(int64_t)(p.reverse ? p.nch - 1 - i : i) * p.len]; };
-    int i = 0;
-    for (; i + 16 <= p.nch; i += 16) {  // sixteen loads in flight, then sixteen stores
-        float x[16];
+    const int64_t dd = (int64_t)p.d * p.dv, e = 4 * e4;
+    float run[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* base = e < dd ? (p.base_M ? p.base_M + (int64_t)bh * dd + e : nullptr)
+                               : (p.base_z ? p.base_z + (int64_t)bh * p.d + (e - dd) : nullptr);
+    if (base)
 #pragma unroll
-        for (int u = 0; u < 16; ++u) x[u] = at(i + u);
+        for (int u = 0; u < 4; ++u) run[u] = base[u];
+    float4* r = reinterpret_cast<float4*>(p.rec + (int64_t)bh * p.nch * p.len) + e4;
+    for (int i = 0; i < p.nch; i += G) {
+        float4 x[G];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            at(i + u) = run;
-            run += x[u];
-        }
+        for (int u = 0; u < G; ++u)
+            if (i + u < p.nch) x[u] = r[(int64_t)(p.reverse ? p.nch - 1 - (i + u) : i + u) * n4];
+#pragma unroll
+        for (int u = 0; u < G; ++u)
+            if (i + u < p.nch) {
+                r[(int64_t)(p.reverse ? p.nch - 1 - (i + u) : i + u) * n4] = make_float4(run[0], run[1], run[2], run[3]);
+                run[0] += x[u].x, run[1] += x[u].y, run[2] += x[u].z, run[3] += x[u].w;
+            }
     }
-    for (; i < p.nch; ++i) {
-        const float x = at(i);
-        at(i) = run;
-        run += x;
-    }
-    if (e < dd) {
-        if (p.total_M) p.total_M[(int64_t)bh * dd + e] = run;
-    } else if (p.total_z) {
-        p.total_z[(int64_t)bh * p.d + (e - dd)] = run;
-    }
+    float* tot = e < dd ? (p.total_M ? p.total_M + (int64_t)bh * dd + e : nullptr)
+                        : (p.total_z ? p.total_z + (int64_t)bh * p.d + (e - dd) : nullptr);
+    if (tot)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) tot[u] = run[u];
 }
 
 size_t dq_smem(int d, int dv) {
@@ -516,7 +516,8 @@ size_t bwd_workspace_floats(int64_t BH, int64_t T, int d, int dv, size_t* off_re
 }
 
 cudaError_t launch_scan_states(const ScanParams& p, cudaStream_t s) {
-    dim3 grid((unsigned)((p.len + NT - 1) / NT), p.BH);
+    if (p.len % 8 != 0) return cudaErrorInvalidValue;  // d, dv multiples of 8
+    dim3 grid((unsigned)((p.len / 4 + NT - 1) / NT), p.BH);
     scan_states_kernel<<<grid, NT, 0, s>>>(p);
     return cudaGetLastError();
 }

@@ -43,22 +43,24 @@ struct ScanParams {
     bool reverse;          // false: record c <- base + sum_{c' < c}; true: base + sum_{c' > c}
 };
 
-// Tensor-core chunk kernels (la_bwd_tc.cu), bf16 storage, d and dv in {64, 128}: one block
-// per (64-token chunk, b*H + h). states / rev: the records above (the state before each
-// chunk; the chunk sums phi(Q)^T G and phi(Q)^T e, then after the reverse scan the state
-// gradient from every token after the chunk); G: g_t as bf16 high parts [B*H][T][dv] and,
-// right after them, the bf16 remainders (both in the G region, sized for f32); E: e_t.
+// Tensor-core sweeps (la_bwd_tc.cu), bf16 storage, d and dv in {64, 128}: one block per
+// (range of cpr 64-token chunks, b*H + h); nr ranges per head. states: one record per range
+// (the state before it, after the prefix scan); rev: one record per range (its sums
+// phi(Q)^T G and phi(Q)^T e from the dq sweep; after the reverse scan, the state gradient
+// from every token after the range). Dn, E: D_t and e_t per token [B*H][T], written by the
+// dq sweep and read by the dk/dv sweep.
 struct BwdTcParams {
     void* dq;
     void* dk;
     void* dv;
     const float* states;
     float* rev;
-    void* G;
+    float* Dn;
     float* E;
     int B, H;
     int64_t T;
     int d, dv_dim, nch;
+    int nr, cpr;
     int64_t rec;
     float eps;
     int* status;
@@ -67,8 +69,9 @@ struct BwdTcParams {
 cudaError_t launch_bwd_dq_tc(const BwdTcParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_tc(const BwdTcParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                               const CUtensorMap& mv, const CUtensorMap& mg, const CUtensorMap& mgl,
-                               cudaStream_t s);
+                               const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t s);
+// blocks of both sweeps that fit on one SM at once (shared memory, registers, TMEM)
+int bwd_sweep_occupancy(int d, int dv);
 
 size_t bwd_workspace_floats(int64_t BH, int64_t T, int d, int dv, size_t* off_rev, size_t* off_G, size_t* off_E);
 cudaError_t launch_scan_states(const ScanParams& p, cudaStream_t s);

@@ -198,7 +198,7 @@ static cudaError_t launch_parts_tc_t(const PartsParams& p, const CUtensorMap& mk
                                      cudaStream_t s) {
     using L = PartsLayout<D, DV>;
     auto fn = parts_tc_kernel<D, DV>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    cudaError_t e = set_smem_attrs(reinterpret_cast<const void*>(fn), L::ALLOC);
     if (e != cudaSuccess) return e;
     dim3 grid(p.nparts, p.B * p.H);
     fn<<<grid, PARTS_THREADS, L::ALLOC, s>>>(mk, mv, p);

@@ -10,6 +10,15 @@ constexpr int ATOM = 64 * 128;         // one 64-row, 128-byte-wide swizzle bloc
 constexpr int KROWS = 80;              // forward K tile rows: 64 keys, z row, 15 zero rows
 constexpr int ATOMK = KROWS * 128;
 
+// Dynamic shared memory of a kernel, with the largest shared-memory carveout preferred:
+// without that preference the driver may size the carveout for one block and keep a
+// second block of a kernel that fits two per SM off the SM.
+static inline cudaError_t set_smem_attrs(const void* fn, int bytes) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // Round the dynamic shared-memory base up to 1024 bytes (the 128-byte swizzle repeats
 // every 1024 bytes). Plain pointer arithmetic on the __shared__ array, so the compiler
 // still knows every derived pointer is a shared-memory address (ld/st.shared rather
