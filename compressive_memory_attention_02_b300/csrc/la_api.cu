@@ -240,8 +240,8 @@ static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dt
     }
     if (ws_avail < alias_bytes) return pl;
     // range 0's share of the chunks: range 1 re-forms their state first (measured optimum:
-    // 70% at d = 128, 64% at d = 64, where a chunk's fixed costs weigh more)
-    const int pct = env_int("LA_FWD_SPLIT_PCT", d >= 128 ? 70 : 64);
+    // 68% at d = 128, 66% at d = 64, where a chunk's fixed costs weigh more)
+    const int pct = env_int("LA_FWD_SPLIT_PCT", d >= 128 ? 68 : 66);
     int64_t split = (nch * pct + 50) / 100;
     split = std::max<int64_t>(1, std::min<int64_t>(split, nch - 1));
     pl.nranges = 2;

@@ -50,8 +50,8 @@ def bwd(q, k, v, dout, M_in=None, z_in=None, dM_out=None, dz_out=None, eps=1e-6,
     ws = torch.empty(nws, dtype=torch.uint8, device=q.device)
     la.la_causal_bwd_ex(q, k, v, dout, M_in, z_in, dM_out, dz_out, dq, dk, dvv, dM_in, dz_in, B, H, T, d, dv, eps,
                         dtype_code(q), ws, nws)
-    # bf16 with d, dv in {64, 128}: the tensor-core kernels (chunk sums, scan, dq, reverse scan,
-    # dk and dv); otherwise the float32 SIMT kernels (one more launch)
+    # bf16 with d, dv in {64, 128}: the tensor-core sweeps (range key-value sums, scan, dq sweep,
+    # reverse scan, dk/dv sweep); otherwise the float32 SIMT kernels (one more launch)
     tc = q.dtype == torch.bfloat16 and d in (64, 128) and dv in (64, 128) and not os.environ.get("LA_FORCE_SIMT")
     assert la.la_last_launch_count() == (5 if tc else 6)
     check_status()
@@ -126,6 +126,17 @@ def test_bf16_tensor_core_edges(case, d):
     ref = oracle.causal_bwd(q, k, v, _values(dout))
     got = bwd(to_dev(q), to_dev(k), to_dev(v), to_dev(dout))
     _compare(got, ref, TOL_BF16, f"{case}_d{d}")
+
+
+@pytest.mark.parametrize("cpr", [1, 2, 3, 5])
+@pytest.mark.parametrize("d,dv,T", [(64, 64, 333), (128, 128, 449), (64, 128, 257)])
+def test_bf16_sweeps_over_forced_range_lengths(monkeypatch, cpr, d, dv, T):
+    """The sweeps' ranges of cpr chunks (the default plan puts a whole short sequence in one range):
+    every range boundary hands the state (prefix scan) and the state gradient (reverse scan) over
+    through the per-range records, and the last range is ragged."""
+    monkeypatch.setenv("LA_BWD_CPR", str(cpr))
+    got, ref = _case(590 + cpr + d + T, 1, 3, T, d, dv, "bf16", 0.5)
+    _compare(got, ref, TOL_BF16, f"ranges_cpr{cpr}_d{d}_dv{dv}_T{T}")
 
 
 def test_bf16_tensor_core_and_simt_paths_agree(monkeypatch):
