@@ -455,9 +455,10 @@ def _graph_time(call, reps, dev):
 
 
 def run_modes(dev):
-    """The other workloads: prefill (B=1 H=8 T=1,048,576, final state and last output), the
-    training-style forward and backward (B=4 H=16 T=4096 d=dv=64, one call each) and decode
-    steps (256 streams x 32 heads). Kernel-only device time."""
+    """The other workloads: the segmented workload as one call over all its tokens, prefill
+    (B=1 H=8 T=1,048,576, final state and last output), the training-style forward and
+    backward (B=4 H=16 T=4096 d=dv=64, one call each) and decode steps (256 streams x 32
+    heads). Kernel-only device time."""
     import torch
 
     import compressive_memory_attention_02_b300 as la
@@ -465,6 +466,30 @@ def run_modes(dev):
     hbm_peak, _, src = peaks()
     bf = lambda a: torch.from_numpy(a).view(torch.bfloat16).to(dev)
     res = {}
+
+    # the segmented workload's tokens in one call (chaining the segment calls gives the same
+    # outputs up to rounding): the chunked kernel without a fill and drain every 2048 tokens
+    w = synthetic.WORKLOADS["segmented"]
+    B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
+    q, k, v = (bf(synthetic.normal(replica_seed(w, 0), tid, (B, H, T, x), w.scale, "bf16"))
+               for tid, x in ((synthetic.TID_Q, d), (synthetic.TID_K, d), (synthetic.TID_V, dv)))
+    out = torch.empty(B, H, T, dv, dtype=torch.bfloat16, device=dev)
+    M = torch.empty(B, H, d, dv, device=dev)
+    z = torch.empty(B, H, d, device=dev)
+    nws = la.la_causal_fwd_workspace_size(B, H, T, d, dv, w.chunk, la.LA_BF16)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+    ms = _graph_time(lambda: la.la_causal_fwd_ex(q, k, v, out, None, None, M, z, B, H, T, d, dv, w.chunk, w.eps,
+                                                 la.LA_BF16, None, ws, nws), 5, dev)
+    assert la.la_get_last_device_status() == la.LA_OK
+    byt = B * H * T * (2 * d + 2 * dv) * 2 + B * H * (d * dv + d) * 4
+    res["segmented_one_call"] = {
+        "workload": f"B={B} H={H} T={T} d=dv={d} bf16 in one call (the headline runs it as 16 chained "
+                    f"segment calls), zero initial state, M_out written",
+        "value": round(B * T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(ms, 4),
+        "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                     "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs"}}
+    del q, k, v, out, ws
 
     w = synthetic.WORKLOADS["prefill"]
     B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
