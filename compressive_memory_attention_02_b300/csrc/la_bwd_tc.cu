@@ -55,11 +55,6 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
     lo = pack_bf16(a - bf16lo(hi), b - bf16hi(hi));
 }
 
-// byte offset of bf16 element (row, col) of a tile with 64-column blocks `bstride` bytes apart
-__device__ __forceinline__ uint32_t tile_off(int row, int col, int bstride) {
-    return (col >> 6) * bstride + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2;
-}
-
 // Row `row`, columns c0..c0+15 of a swizzled bf16 tile, as two 16-byte stores.
 __device__ __forceinline__ void tile_put16(uint8_t* tile, int row, int c0, int bstride, const uint32_t* w) {
     uint8_t* r = tile + (c0 >> 6) * bstride + row * 128;
@@ -140,25 +135,8 @@ __device__ __forceinline__ void record_to_state(const float* rec, uint32_t tacc,
     tmem_wait_st();
 }
 
-template <int D, int DV>
-__device__ __forceinline__ void state_to_tile(uint32_t tacc, uint8_t* tile, int bstride, int warp, int lane) {
-    const int q = warp - 4;
-    if (q < 0 || 32 * q >= D) return;
-    const int i = 32 * q + lane;
-    const uint32_t ta = tacc + ((uint32_t)(32 * q) << 16);
-#pragma unroll 1
-    for (int j0 = 0; j0 < DV; j0 += 16) {
-        float x[16];
-        ld16f(ta + j0, x);
-        uint32_t w[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
-        tile_put16(tile, i, j0, bstride, w);
-    }
-}
-
-// The same copy split over every warp whose lane quarter holds state rows: quarter w % 4,
-// column half w / 4.
+// TMEM state -> its bf16 tile, split over every warp whose lane quarter holds state rows:
+// quarter w % 4, column half w / 4.
 template <int D, int DV>
 __device__ __forceinline__ void state_to_tile_split(uint32_t tacc, uint8_t* tile, int bstride, int warp, int lane) {
     const int q = warp & 3, hf = warp >> 2;
