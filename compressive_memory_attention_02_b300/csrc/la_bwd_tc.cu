@@ -23,10 +23,11 @@
 // la_bwd.cu over one record per range (the key-value sums of parts_tc, and the state-
 // gradient sums of the first sweep).
 //
-// G, P and dA are formed in f32; each enters its products as two bf16 operands, the high
-// part and the rounded remainder (x = hi + lo to ~16 bits), so that the cancellations in
-// dq (M g + e z against the intra-chunk sum, and g . v_j + e inside dA) act on f32-accurate
-// values. phi, V, dout and the carried states enter as bf16.
+// G and dA are formed in f32 and enter their products as two bf16 operands, the high part
+// and the rounded remainder (x = hi + lo to ~16 bits), so that the cancellations in dq
+// (M g + e z against the intra-chunk sum, and g . v_j + e inside dA) act on f32-accurate
+// values. phi, V, dout, the carried states and P enter as bf16 (P reaches dv alone, whose
+// sums do not cancel the way dq's do).
 //
 // 256 threads; warp w may touch only TMEM lane quarter w % 4. Per-token passes use warps 0
 // and 1 (lanes 0-63 = the chunk's tokens), state copies warps 4-7. Thread 0 issues the TMA
@@ -629,7 +630,7 @@ struct DkvLayout {
     // data, so the rows an M = 128 MMA reads past each of them stay inside the allocation
     static constexpr int QT = 0;                          // phi(Q), 2 stages
     static constexpr int KT = QT + 2 * (D / 64) * ATOM;   // phi(K), 2 stages
-    static constexpr int PT = KT + 2 * (D / 64) * ATOM;   // P^T [64 keys][64 queries] high, then low
+    static constexpr int PT = KT + 2 * (D / 64) * ATOM;   // P^T [64 keys][64 queries] bf16 (+ one atom read past)
     static constexpr int AT = PT + 2 * ATOM;              // dA^T (masked, + e) high, then low
     static constexpr int VT = AT + 2 * ATOM;              // V, DV/64 atoms
     static constexpr int OT = VT + DV / 64 * ATOM;        // dout, DV/64 atoms
@@ -802,13 +803,14 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         ok = block_wait(&bars[B_O], idx & 1, abort_flag, p.status);
         if (!ok) break;
         ++pend[B_O].waited;
-        // ---- G = dout / D: high parts into [G; R], low parts; column halves
+        // ---- G = dout / D: high parts into [G; R], low parts; every warp (no TMEM access):
+        // thread tid takes query row tid % 64 and a quarter of the DV columns
         if (!tok && act < D) rn[act] = rc[act];  // r before this chunk, completed during g2
-        if (tok) {
-            const int t = trow;
+        {
+            const int t = tid & 63, cq = tid >> 6;
             const float rd = t < valid ? 1.f / dc[t] : 0.f;
 #pragma unroll 1
-            for (int j0 = thalf * (DV / 2); j0 < (thalf + 1) * (DV / 2); j0 += 16) {
+            for (int j0 = cq * (DV / 4); j0 < (cq + 1) * (DV / 4); j0 += 16) {
                 float o[16];
                 tile_get8(sm + L::OT, t, j0, ATOM, o);
                 tile_get8(sm + L::OT, t, j0 + 8, ATOM, o + 8);
@@ -858,8 +860,8 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         ++mph, ++pend[B_MMA].waited;
         tc_fence_after();
         if (tid == 0 && more) load_v(idx + 1);  // V's only reader (g1) is done
-        // ---- mask: P^T and dA^T + e, masked to queries at or after the key (hi, lo); key
-        // rows, query-column halves
+        // ---- mask: P^T (bf16: it enters dv alone) and dA^T + e (high and low parts), masked to
+        // queries at or after the key; key rows, query-column halves
         if (tok) {
             const int j = trow, hf = thalf;
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
@@ -868,17 +870,16 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
             ld32f(tmem + L::TA + lb + 32 * hf, a);
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
-                uint32_t ph[8], pl[8], ah[8], al[8];
+                uint32_t ph[8], ah[8], al[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const int c = 16 * g + 2 * q, tq = 32 * hf + c;
                     const bool m0 = tq >= j, m1 = tq + 1 >= j;
-                    split2(m0 ? sv[c] : 0.f, m1 ? sv[c + 1] : 0.f, ph[q], pl[q]);
+                    ph[q] = pack_bf16(m0 ? sv[c] : 0.f, m1 ? sv[c + 1] : 0.f);
                     split2(m0 ? a[c] + ec[tq] : 0.f, m1 ? a[c + 1] + ec[tq + 1] : 0.f, ah[q], al[q]);
                 }
                 const int col = 32 * hf + 16 * g;
                 tile_put16(sm + L::PT, j, col, ATOM, ph);
-                tile_put16(sm + L::PT + ATOM, j, col, ATOM, pl);
                 tile_put16(sm + L::AT, j, col, ATOM, ah);
                 tile_put16(sm + L::AT + ATOM, j, col, ATOM, al);
             }
@@ -893,9 +894,8 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
             constexpr uint32_t id_kq = idesc_bf16(128, D, 0, 1);
 #pragma unroll
             for (int ks = 0; ks < CH / 16; ++ks) {
-                // P^T G with both split: hi.hi + lo.hi + hi.lo
+                // P^T G with G split: P^T G_hi + P^T G_lo
                 mma_bf16_ss(tmem + L::TS, dPk + off(ks * 32), dGHm + off(ks * 2048), id_vg, ks != 0);
-                mma_bf16_ss(tmem + L::TS, dPk + off(ATOM + ks * 32), dGHm + off(ks * 2048), id_vg, 1);
                 mma_bf16_ss(tmem + L::TS, dPk + off(ks * 32), dGLm + off(ks * 2048), id_vg, 1);
                 mma_bf16_ss(tmem + L::TK, dAk + off(ks * 32), dQm + off(ks * 2048), id_kq, 1);
                 mma_bf16_ss(tmem + L::TK, dAk + off(ATOM + ks * 32), dQm + off(ks * 2048), id_kq, 1);
