@@ -553,10 +553,13 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
         if (forced > 0) {
             cpr = forced < nch ? forced : nch;
         } else {
-            for (int64_t c = nch; c >= 1; --c) {
-                const int64_t nr_c = ceil_div(nch, c);
-                const int64_t cost = ceil_div(BH * nr_c, slots) * (c + 1);
-                if (best < 0 || cost < best) best = cost, cpr = c;
+            // by number of ranges per head: beyond a few waves of blocks more ranges only add
+            // waves, so the search stops at 4 x slots ranges
+            const int64_t max_nr = std::min<int64_t>(nch, 4 * slots);
+            for (int64_t nr_c = 1; nr_c <= max_nr; ++nr_c) {
+                const int64_t c = ceil_div(nch, nr_c);
+                const int64_t cost = ceil_div(BH * ceil_div(nch, c), slots) * (c + 1);
+                if (best < 0 || cost < best || (cost == best && c > cpr)) best = cost, cpr = c;
             }
         }
         const int64_t nr = ceil_div(nch, cpr);
