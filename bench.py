@@ -550,7 +550,7 @@ def run_modes(dev):
     res["train_bwd"] = {"workload": f"B={B} H={H} T={T} d=dv={d} bf16, dout ~ N(0,1), dq, dk, dv + dM_in, dz_in",
                         "value": round(B * T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(ms, 5),
                         "launches": la.la_last_launch_count(),
-                        "kernels": "tensor-core sweeps (range key-value sums, scan, dq sweep, reverse scan, dk/dv sweep)",
+                        "kernels": "tensor-core sweeps (range key-value sums, dq sweep, dk/dv sweep; ordered scans past eight ranges per head)",
                         "roofline": {"bound": "hbm", "achieved": round(byt / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
                                      "unit": "GB/s", "frac": round(byt / (ms / 1e3) / 1e9 / hbm_peak, 4),
                                      "per_call_bytes": byt, "peak_source": f"{src} hbm_gbs",

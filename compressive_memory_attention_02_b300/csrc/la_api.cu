@@ -533,9 +533,9 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
                     env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31) && aligned16(dq) &&
                     aligned16(dk) && aligned16(dv);  // the gradients are stored in 16-byte vectors
     if (tc) {
-        // tensor-core sweeps over ranges of 64-token chunks: the key-value sum of every range
-        // (parts_tc), the prefix scan over ranges, the dq sweep (with D_t, e_t and each
-        // range's sums of the state gradient), the reverse scan, then the dk/dv sweep
+        // tensor-core sweeps over ranges of 64-token chunks: the key-value sum of each range
+        // (parts_tc), the dq sweep (with D_t, e_t and each range's sums of the state
+        // gradient), then the dk/dv sweep
         const Strides st = contiguous(H, T, d, dv_dim);
         CUtensorMap mq, mk, mv, mdo;
         if (!make_map(&mq, q, d, T, H, B, st.q_st, st.q_sh, st.q_sb) ||
@@ -563,29 +563,42 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* dou
             }
         }
         const int64_t nr = ceil_div(nch, cpr);
-        PartsParams pp{};
-        pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv_dim, pp.rec_M = rec, pp.rec_z = rec;
-        pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv_dim, pp.part_len = cpr * BWD_CH, pp.nparts = (int)nr;
-        pp.eps = eps, pp.st = st, pp.status = ds->status;
-        if ((rc = cuda_rc(launch_parts_tc(pp, mk, mv, stream)))) return rc;
-        ++t_launches;
-        ScanParams sp{};
-        sp.rec = wsf, sp.base_M = M_in, sp.base_z = z_in, sp.BH = (int)BH, sp.nch = (int)nr;
-        sp.d = d, sp.dv = dv_dim, sp.len = rec, sp.reverse = false;
-        if ((rc = cuda_rc(launch_scan_states(sp, stream)))) return rc;
-        ++t_launches;
+        // up to BWD_FOLD_RANGES ranges per head each block adds up the records before (after)
+        // its range itself; beyond that ordered scans over the ranges do it once, in place
+        const bool folded = nr <= BWD_FOLD_RANGES;
+        const int64_t nparts = folded ? nr - 1 : nr;  // a folded plan never reads the last range's sum
+        if (nparts > 0) {
+            PartsParams pp{};
+            pp.k = k, pp.v = v, pp.dst_M = wsf, pp.dst_z = wsf + (size_t)d * dv_dim, pp.rec_M = rec, pp.rec_z = rec;
+            pp.B = B, pp.H = H, pp.T = T, pp.d = d, pp.dv = dv_dim, pp.part_len = cpr * BWD_CH,
+            pp.nparts = (int)nparts;
+            pp.eps = eps, pp.st = st, pp.status = ds->status;
+            if ((rc = cuda_rc(launch_parts_tc(pp, mk, mv, stream)))) return rc;
+            ++t_launches;
+        }
+        if (!folded) {
+            ScanParams sp{};
+            sp.rec = wsf, sp.base_M = M_in, sp.base_z = z_in, sp.BH = (int)BH, sp.nch = (int)nr;
+            sp.d = d, sp.dv = dv_dim, sp.len = rec, sp.reverse = false;
+            if ((rc = cuda_rc(launch_scan_states(sp, stream)))) return rc;
+            ++t_launches;
+        }
         BwdTcParams tp{};
         tp.dq = dq, tp.dk = dk, tp.dv = dv, tp.states = wsf, tp.rev = wsf + off_rev;
+        if (folded)
+            tp.M_in = M_in, tp.z_in = z_in, tp.dM_out = dM_out, tp.dz_out = dz_out, tp.dM_in = dM_in, tp.dz_in = dz_in;
         tp.Dn = wsf + off_G, tp.E = wsf + off_E;  // D_t in the (here unused) G region
         tp.B = B, tp.H = H, tp.T = T, tp.d = d, tp.dv_dim = dv_dim, tp.nch = (int)nch;
-        tp.nr = (int)nr, tp.cpr = (int)cpr, tp.rec = rec, tp.eps = eps, tp.status = ds->status;
+        tp.nr = (int)nr, tp.cpr = (int)cpr, tp.scanned = !folded, tp.rec = rec, tp.eps = eps, tp.status = ds->status;
         if ((rc = cuda_rc(launch_bwd_dq_tc(tp, mq, mk, mv, mdo, stream)))) return rc;
         ++t_launches;
-        ScanParams rp{};
-        rp.rec = wsf + off_rev, rp.base_M = dM_out, rp.base_z = dz_out, rp.total_M = dM_in, rp.total_z = dz_in;
-        rp.BH = (int)BH, rp.nch = (int)nr, rp.d = d, rp.dv = dv_dim, rp.len = rec, rp.reverse = true;
-        if ((rc = cuda_rc(launch_scan_states(rp, stream)))) return rc;
-        ++t_launches;
+        if (!folded) {
+            ScanParams rp{};
+            rp.rec = wsf + off_rev, rp.base_M = dM_out, rp.base_z = dz_out, rp.total_M = dM_in, rp.total_z = dz_in;
+            rp.BH = (int)BH, rp.nch = (int)nr, rp.d = d, rp.dv = dv_dim, rp.len = rec, rp.reverse = true;
+            if ((rc = cuda_rc(launch_scan_states(rp, stream)))) return rc;
+            ++t_launches;
+        }
         if ((rc = cuda_rc(launch_bwd_dkdv_tc(tp, mq, mk, mv, mdo, stream)))) return rc;
         ++t_launches;
         return LA_OK;

@@ -44,23 +44,36 @@ struct ScanParams {
 };
 
 // Tensor-core sweeps (la_bwd_tc.cu), bf16 storage, d and dv in {64, 128}: one block per
-// (range of cpr 64-token chunks, b*H + h); nr ranges per head. states: one record per range
-// (the state before it, after the prefix scan); rev: one record per range (its sums
-// phi(Q)^T G and phi(Q)^T e from the dq sweep; after the reverse scan, the state gradient
-// from every token after the range). Dn, E: D_t and e_t per token [B*H][T], written by the
-// dq sweep and read by the dk/dv sweep.
+// (range of cpr 64-token chunks, b*H + h); nr ranges per head; rev gets one record per
+// range from the dq sweep (its sums phi(Q)^T G and phi(Q)^T e). Two ways to carry the
+// state between ranges:
+//   folded (scanned == 0, nr <= BWD_FOLD_RANGES): states holds the key-value sums of ranges
+//     0 .. nr-2 ([B*H][nr-1] records from parts_tc); a block adds M_in, z_in (or dM_out,
+//     dz_out) and the records before (after) its range itself, and range 0 of the dk/dv
+//     sweep writes dM_in, dz_in. Any of these six may be null (zero / not written).
+//   scanned (scanned == 1): states and rev are [B*H][nr] records already turned into the
+//     state before / the state gradient after each range by the ordered scans of
+//     la_bwd.cu, which also take the caller's arrays; the six pointers are unused.
+// Dn, E: D_t and e_t per token [B*H][T], written by the dq sweep and read by the dk/dv sweep.
+constexpr int BWD_FOLD_RANGES = 8;
 struct BwdTcParams {
     void* dq;
     void* dk;
     void* dv;
     const float* states;
     float* rev;
+    const float* M_in;
+    const float* z_in;
+    const float* dM_out;
+    const float* dz_out;
+    float* dM_in;
+    float* dz_in;
     float* Dn;
     float* E;
     int B, H;
     int64_t T;
     int d, dv_dim, nch;
-    int nr, cpr;
+    int nr, cpr, scanned;
     int64_t rec;
     float eps;
     int* status;

@@ -19,9 +19,12 @@
 //                   share of the state gradient (sum phi(Q)^T G, sum phi(Q)^T e)
 //   bwd_dkdv_sweep  one block per (range, b*H + h), chunks in reverse, (R, r) carried the
 //                   same way: G re-formed from dout and D_t, dk and dv
-// The state before each range and (R, r) after it come from the ordered scans of
-// la_bwd.cu over one record per range (the key-value sums of parts_tc, and the state-
-// gradient sums of the first sweep).
+// The state before a range is the initial state plus the key-value sums of the ranges
+// before it (parts_tc writes one record per range), and (R, r) after it the gradient of
+// the final state plus the state-gradient sums of the ranges after it (one record per
+// range from the first sweep). With a few ranges per head each block adds them up in
+// order in its prologue and range 0 of the second sweep ends with the gradient of the
+// initial state; with more, the ordered scans of la_bwd.cu do it between the launches.
 //
 // G and dA are formed in f32 and enter their products as two bf16 operands, the high part
 // and the rounded remainder (x = hi + lo to ~16 bits), so that the cancellations in dq
@@ -110,30 +113,63 @@ __device__ __forceinline__ void ld32f(uint32_t taddr, float* x) {
 __device__ __forceinline__ bool is_token_warp(int warp) { return (warp & 2) == 0; }
 __device__ __forceinline__ int aux_index(int warp, int lane) { return (warp >> 2) * 64 + (warp & 1) * 32 + lane; }
 
-// A carried state (D x DV, f32, lanes = rows) between a record, TMEM and its bf16 tile.
-// Warps 4 .. 4 + D/32 - 1 take lane quarter warp - 4, all DV columns.
+// A carried state (D x DV, f32, lanes = rows) between memory, TMEM and its bf16 tile.
+//
+// sum_to_state: base (the caller's [D][DV] state, any alignment, may be null) plus the nrec
+// records recs + k * rstride (workspace, 16-byte aligned) into TMEM and the tile. Warps w
+// and w + 4 share lane quarter w % 4 and take one half of the columns each; the records
+// are read two at a time so that their loads are in flight together.
 template <int D, int DV>
-__device__ __forceinline__ void record_to_state(const float* rec, uint32_t tacc, uint8_t* tile, int bstride,
-                                                int warp, int lane) {
-    const int q = warp - 4;
-    if (q < 0 || 32 * q >= D) return;
+__device__ __forceinline__ void sum_to_state(const float* base, const float* recs, int64_t rstride, int nrec,
+                                             uint32_t tacc, uint8_t* tile, int bstride, int warp, int lane) {
+    const int q = warp & 3, half = warp >> 2;
+    if (32 * q >= D) return;
     const int i = 32 * q + lane;
     const uint32_t ta = tacc + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1
-    for (int j0 = 0; j0 < DV; j0 += 16) {
+    for (int j0 = half * (DV / 2); j0 < (half + 1) * (DV / 2); j0 += 16) {
+        float x[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = base ? base[(int64_t)i * DV + j0 + e] : 0.f;
+        const float* rec = recs + (int64_t)i * DV + j0;
+        int k = 0;
+#pragma unroll 1
+        for (; k + 2 <= nrec; k += 2) {
+            float4 a[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                a[e] = __ldg(reinterpret_cast<const float4*>(rec + k * rstride) + e);
+                a[4 + e] = __ldg(reinterpret_cast<const float4*>(rec + (k + 1) * rstride) + e);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[4 * e] += a[e].x + a[4 + e].x, x[4 * e + 1] += a[e].y + a[4 + e].y;
+                x[4 * e + 2] += a[e].z + a[4 + e].z, x[4 * e + 3] += a[e].w + a[4 + e].w;
+            }
+        }
+        if (k < nrec) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(rec + k * rstride) + e);
+                x[4 * e] += a.x, x[4 * e + 1] += a.y, x[4 * e + 2] += a.z, x[4 * e + 3] += a.w;
+            }
+        }
         uint32_t r[16], w[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(rec + (int64_t)i * DV + j0 + e));
-            r[e] = __float_as_uint(a.x), r[e + 1] = __float_as_uint(a.y);
-            r[e + 2] = __float_as_uint(a.z), r[e + 3] = __float_as_uint(a.w);
-        }
+        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(x[e]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+        for (int e = 0; e < 8; ++e) w[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
         tmem_st16(ta + j0, r);
         tile_put16(tile, i, j0, bstride, w);
     }
     tmem_wait_st();
+}
+
+// The same sum for the vector part (z or r) of feature i: base[i] + recs[k * rstride + i].
+__device__ __forceinline__ float sum_vec(const float* base, const float* recs, int64_t rstride, int nrec, int i) {
+    float a = base ? base[i] : 0.f;
+    for (int k = 0; k < nrec; ++k) a += recs[k * rstride + i];
+    return a;
 }
 
 // TMEM state -> its bf16 tile, split over every warp whose lane quarter holds state rows:
@@ -155,6 +191,22 @@ __device__ __forceinline__ void state_to_tile_split(uint32_t tacc, uint8_t* tile
 #pragma unroll
         for (int e = 0; e < 8; ++e) w[e] = pack_bf16(x[16 + 2 * e], x[16 + 2 * e + 1]);
         tile_put16(tile, i, j0 + 16, bstride, w);
+    }
+}
+
+// TMEM state -> the caller's [D][DV] array (any alignment), warps 4 .. 4 + D/32 - 1.
+template <int D, int DV>
+__device__ __forceinline__ void state_to_array(uint32_t tacc, float* dst, int warp, int lane) {
+    const int q = warp - 4;
+    if (q < 0 || 32 * q >= D) return;
+    const int i = 32 * q + lane;
+    const uint32_t ta = tacc + ((uint32_t)(32 * q) << 16);
+#pragma unroll 1
+    for (int j0 = 0; j0 < DV; j0 += 16) {
+        float x[16];
+        ld16f(ta + j0, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dst[(int64_t)i * DV + j0 + e] = x[e];
     }
 }
 
@@ -369,11 +421,15 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         load_v(0);
         load_o(0);
     }
-    // the state before the range: M into TMEM and its bf16 tile, z; the range's sums start at 0
-    const float* srec = p.states + rec_i * p.rec;
-    record_to_state<D, DV>(srec, tmem + L::TM, sm + L::VM + ATOM, L::VMB, warp, lane);
+    // the state before the range (the initial state plus the key-value sums of the ranges
+    // before it; one record when scanned): M into TMEM and its bf16 tile, z; the range's
+    // sums start at 0
+    const float* recs = p.scanned ? p.states + rec_i * p.rec : p.states + (int64_t)bh * (p.nr - 1) * p.rec;
+    const int nbefore = p.scanned ? 1 : r;
+    const float* Mb = p.M_in ? p.M_in + (int64_t)bh * D * DV : nullptr;
+    sum_to_state<D, DV>(Mb, recs, p.rec, nbefore, tmem + L::TM, sm + L::VM + ATOM, L::VMB, warp, lane);
     if (tid < D) {
-        zf[tid] = srec[D * DV + tid];
+        zf[tid] = sum_vec(p.z_in ? p.z_in + (int64_t)bh * D : nullptr, recs + D * DV, p.rec, nbefore, tid);
         rsum[tid] = 0.f;
     }
     fence_proxy_async_smem();
@@ -754,10 +810,13 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         load_v(0);
         load_o(0);
     }
-    // (R, r) after the range: R into TMEM and its bf16 tile
-    const float* rrec = p.rev + rec_i * p.rec;
-    record_to_state<D, DV>(rrec, tmem + L::TRR, sm + L::GR + ATOM, L::GRB, warp, lane);
-    if (tid < D) rv[tid] = rrec[D * DV + tid];
+    // (R, r) after the range (the gradient of the final state plus the sums of the ranges
+    // after it; one record when scanned): R into TMEM and its bf16 tile
+    const float* rrecs = p.rev + (p.scanned ? rec_i : rec_i + 1) * p.rec;
+    const int nafter = p.scanned ? 1 : p.nr - 1 - r;
+    const float* Rb = p.dM_out ? p.dM_out + (int64_t)bh * D * DV : nullptr;
+    sum_to_state<D, DV>(Rb, rrecs, p.rec, nafter, tmem + L::TRR, sm + L::GR + ATOM, L::GRB, warp, lane);
+    if (tid < D) rv[tid] = sum_vec(p.dz_out ? p.dz_out + (int64_t)bh * D : nullptr, rrecs + D * DV, p.rec, nafter, tid);
     if (!tok && act >= 64 && n > 0) {
         float dd, ee;
         load_de(0, dd, ee);
@@ -964,7 +1023,13 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         fence_proxy_async_smem();
         sync_tc();
     }
-    if (!ok && tid == 0) drain(bars, pend, NB);
+    if (ok && r == 0 && n > 0 && !p.scanned) {
+        // range 0 has added every chunk's share: (R, r) is now the gradient of the initial state
+        if (p.dM_in) state_to_array<D, DV>(tmem + L::TRR, p.dM_in + (int64_t)bh * D * DV, warp, lane);
+        if (p.dz_in && tid < D) p.dz_in[(int64_t)bh * D + tid] = rv[(n & 1) * D + tid];
+    } else if (!ok && tid == 0) {
+        drain(bars, pend, NB);
+    }
     sync_tc();
     if (warp == 0) tmem_dealloc(tmem, L::NCOL);
 }
