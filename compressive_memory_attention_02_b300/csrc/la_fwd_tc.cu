@@ -14,6 +14,15 @@
 // too: phi(K_c)^T (d x 64) times a constant 64 x 16 tile of ones adds the column sums
 // of phi(K_c) to a 16-column f32 accumulator (every column the same; column 0 is read).
 //
+// At dv = 64 the spare lanes 64-127 of the M = 128 products carry the normaliser instead:
+// every V stage is followed by an atom of ones, so rows 64-127 of the V^T operand are 1.
+// The update then adds the column sums of phi(K_c) to lanes 64-127 of M^T (z^T, with z_in
+// placed there at the start), the bf16 re-cast copies z^T into lanes 64-95 of the inter
+// operand, so the inter MMA leaves phi(q_t).z_{c-1} in lanes 64-95 of O^T and PV adds
+// sum_j P_tj there: lane 64 of O^T is den_t - eps. No key-sum MMA, no z row in the K
+// tile (S' is 64 x 64) and no row sums in the P pass; the E warps of lane quarter 2 form
+// 1/den. (The row sum is then over the bf16 P that also enters PV.)
+//
 // One block per (range, head). Warp roles (1024 threads; warp w issues on sub-partition
 // w % 4 and may touch only TMEM lane quarter w % 4):
 //   warp 0        TMA producer: Q, K, V tiles into a 3-stage ring
@@ -51,14 +60,18 @@ constexpr int NFW = 12;  // F warps
 
 template <int D, int DV>
 struct FwdLayout {
+    // dv = 64: the key sum and the denominator ride in lanes 64-127 of the M = 128 products
+    // whose A operand is V^T (rows 64-127 of that operand read an atom of ones kept after
+    // every V stage), so no key-sum MMA and no z row in the K tile
+    static constexpr bool ZL = DV == 64;
     static constexpr int NST = 3;
     static constexpr int QB = D / 64 * ATOM;
     static constexpr int KB = D / 64 * ATOMK;
-    static constexpr int VB = DV / 64 * ATOM;
+    static constexpr int VB = (ZL ? 2 : DV / 64) * ATOM;
     static constexpr int Q0 = 0;
     static constexpr int K0 = Q0 + NST * QB;     // an M=128 read past the last Q atom lands here
     static constexpr int V0 = K0 + NST * KB;
-    static constexpr int PT = V0 + NST * VB;     // P, two buffers; an M=128 read past a 64-wide V tile lands here
+    static constexpr int PT = V0 + NST * VB;     // P, two buffers
     static constexpr int OT = PT + 2 * ATOM;     // out tile
     static constexpr int ONES = OT + DV / 64 * ATOM;  // 16 x 64 bf16 ones (2 KB, 1024-aligned)
     static constexpr int RDEN = ONES + 2048;          // 2 x 64 floats
@@ -149,6 +162,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         reinterpret_cast<uint4*>(sm + L::ONES)[threadIdx.x - 64] = make_uint4(one2, one2, one2, one2);
         fence_proxy_async_smem();
     }
+    if constexpr (L::ZL) {  // the ones atoms after the V stages
+        const uint32_t one2 = 0x3F803F80u;
+        for (int i = threadIdx.x; i < NST * (ATOM / 16); i += FWD_THREADS)
+            *reinterpret_cast<uint4*>(sm + L::V0 + (i / (ATOM / 16)) * L::VB + ATOM + (i % (ATOM / 16)) * 16) =
+                make_uint4(one2, one2, one2, one2);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -189,7 +209,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     } else if (warp == 1) {
         // ======================================================== MMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_s = idesc_bf16(128, KROWS, 0, 0);  // S' = phiQ [phiK; z]^T
+            constexpr uint32_t id_s = idesc_bf16(128, L::ZL ? CH : KROWS, 0, 0);  // S' = phiQ [phiK; z]^T
             constexpr uint32_t id_u = idesc_bf16(128, D, 1, 1);      // M^T += V^T phiK
             constexpr uint32_t id_pv = idesc_bf16(128, CH, 1, 0);    // O^T += V^T P^T
             constexpr uint32_t id_in = idesc_bf16(128, CH, 0, 0);    // O^T = M^T phiQ^T
@@ -218,9 +238,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks)
                     mma_bf16_ss(tmem + TM_M, va + off(ks * 2048), kb + off(ks * 2048), id_u, 1);
+                if constexpr (!L::ZL) {
 #pragma unroll
-                for (int ks = 0; ks < CH / 16; ++ks)
-                    mma_bf16_ss(tmem + TM_Z, kb + off(ks * 2048), d1 + off(ks * 32), id_z, 1);
+                    for (int ks = 0; ks < CH / 16; ++ks)
+                        mma_bf16_ss(tmem + TM_Z, kb + off(ks * 2048), d1 + off(ks * 32), id_z, 1);
+                }
             };
             // S'_m, inter_m, update_m of main chunk m
             auto front = [&](int m) {
@@ -228,7 +250,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 const uint64_t qd = dq0 + off(s * L::QB), kd = dk0 + off(s * L::KB);
                 if (!wait(&phib[s], (g / NST) & 1)) return false;
                 if (m >= 2 && !wait(&s_free[buf], ((m >> 1) - 1) & 1)) return false;
-                if (!wait(zrow_ready, m & 1)) return false;
+                if (!L::ZL && !wait(zrow_ready, m & 1)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -282,8 +304,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const bool has_row = 32 * q < DV;         // warp-uniform
         const bool has_z = 32 * q < D;            // warp-uniform
+        const bool zlanes = L::ZL && q == 2;      // lanes 64-95 of M^T hold z^T (dv = 64)
         auto recast = [&]() {
-            if (!has_row) return;
+            if (!has_row && !zlanes) return;
 #pragma unroll 1
             for (int i0 = 0; i0 < D; i0 += 16) {
                 uint32_t x[16], a[8];
@@ -301,7 +324,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             ok = bar_and(4, 128, mbar_wait(upd_done, upd++ & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            if (u + 1 < n_upd) {
+            if (L::ZL && u + 1 < n_upd) {
+                recast();  // z^T rides along in lanes 64-95
+                tc_fence_before();
+                named_bar_sync(4, 128);
+                if (ct == 0) mbar_arrive(mt_ready);
+            } else if (u + 1 < n_upd) {
                 // the main chunk after this update: its S' reads z from row 64 of its K tile
                 const int mnext = n_agg > 0 ? u : u + 1;
                 if (has_z) {
@@ -317,7 +345,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 named_bar_sync(4, 128);
                 if (ct == 0) mbar_arrive(mt_ready);
             } else if (writes_state) {
-                if (p.z_out && has_z) {
+                if (L::ZL && p.z_out && zlanes) {  // every lane of the quarter holds all of z
+#pragma unroll 1
+                    for (int i0 = 0; i0 < D; i0 += 16) {
+                        uint32_t x[16];
+                        tmem_ld16(tmem + TM_M + lane_base + i0, x);
+                        tmem_wait_ld();
+                        if (lane == 0)
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) p.z_out[(int64_t)bh * D + i0 + e] = __uint_as_float(x[e]);
+                    }
+                } else if (!L::ZL && p.z_out && has_z) {
                     const uint32_t zb = tmem_ld1(tmem + TM_Z + lane_base);
                     tmem_wait_ld();
                     p.z_out[(int64_t)bh * D + j] = __uint_as_float(zb);
@@ -369,7 +407,25 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             }
             tmem_wait_st();
         }
-        if (hf == 0 && 32 * q < D) {
+        if (L::ZL && q == 2) {
+            // z_in (+ range aggregates) as the row z^T in every lane 64-95 of M^T (f32 and
+            // bf16), columns [64hf, 64hf + 64)
+#pragma unroll 1
+            for (int i0 = 64 * hf; i0 < D && i0 < 64 * hf + 64; i0 += 16) {
+                uint32_t x[16], a[8];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float zz = p.z_in ? p.z_in[(int64_t)bh * D + i0 + e] : 0.f;
+                    for (int pp = 0; pp < nws; ++pp) zz += agg[pp * p.rec + D * DV + i0 + e];
+                    x[e] = __float_as_uint(zz);
+                }
+                tmem_st16(tmem + TM_M + lane_base + i0, x);
+                pack16_bf16(x, a);
+                tmem_st8(tmem + TM_A + lane_base + i0 / 2, a);
+            }
+            tmem_wait_st();
+        }
+        if (!L::ZL && hf == 0 && 32 * q < D) {
             // z_in (+ range aggregates) into TMEM; with no state-only chunks before the first
             // main chunk it is also z before that chunk (row 64 of its K tile, stage 0)
             float zz = p.z_in ? p.z_in[(int64_t)bh * D + j] : 0.f;
@@ -385,7 +441,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         named_bar_sync(3, 256);
         if (ct == 0) {
             mbar_arrive(mt_ready);
-            if (n_agg == 0) mbar_arrive(zrow_ready);
+            if (!L::ZL && n_agg == 0) mbar_arrive(zrow_ready);
         }
 
         // Thread l of the warp stores, per stmatrix, row (l % 8) of matrix l / 8: features
@@ -401,6 +457,21 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                                      mbar_wait(&p_full[buf], (m >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
+            if (L::ZL && q == 2) {
+                // lanes 64-95 of O^T all hold phi(q_t).z + sum_j P_tj for token t = 32hf + column;
+                // in the fragment layout threads 0-3 hold the 32 tokens between them
+                uint32_t x[16];
+                tmem_ld16x256_x4(tmem + tm_o(buf) + lane_base + 32 * hf, x);
+                tmem_wait_ld();
+                if (lane < 4) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float* rd = rden + buf * 64 + 32 * hf + 8 * k + 2 * lane;
+                        rd[0] = 1.f / (__uint_as_float(x[4 * k]) + p.eps);
+                        rd[1] = 1.f / (__uint_as_float(x[4 * k + 1]) + p.eps);
+                    }
+                }
+            }
             if (ct == 0) tma_store_wait_read0();  // previous out tile read by the TMA unit
             named_bar_sync(3, 256);
             if (has_row) {
@@ -450,7 +521,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         for (int m = 0; m < n_main; ++m) {
             const int buf = m & 1;
             bool w = mbar_wait(&s_full[buf], (m >> 1) & 1, abort_flag);
-            if (m >= 2) w = w && mbar_wait(&o_free[buf], ((m - 2) >> 1) & 1, abort_flag);  // rden[buf] consumed
+            if (!L::ZL && m >= 2) w = w && mbar_wait(&o_free[buf], ((m - 2) >> 1) & 1, abort_flag);  // rden[buf] consumed
             ok = bar_and(2, 64, w);
             if (!ok) break;
             tc_fence_after();
@@ -478,11 +549,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             };
-            uint32_t zq;
+            uint32_t zq = 0;
             if (q == 0) {  // rows 0-31: keys 32-63 all lie after the row
                 uint32_t x[32];
                 tmem_ld32(srow, x);
-                zq = tmem_ld1(srow + 64);
+                if constexpr (!L::ZL) zq = tmem_ld1(srow + 64);
                 tmem_wait_ld();
                 half(x, 0, true);
 #pragma unroll
@@ -492,12 +563,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 uint32_t x[32], y[32];
                 tmem_ld32(srow, x);
                 tmem_ld32(srow + 32, y);
-                zq = tmem_ld1(srow + 64);
+                if constexpr (!L::ZL) zq = tmem_ld1(srow + 64);
                 tmem_wait_ld();
                 half(x, 0, false);
                 half(y, 1, true);
             }
-            rden[buf * 64 + t] = 1.f / (__uint_as_float(zq) + (f2_lo(rowsum2) + f2_hi(rowsum2)) + p.eps);
+            if constexpr (!L::ZL)  // (dv = 64: the E warps form 1/den from lanes 64-95 of O^T)
+                rden[buf * 64 + t] = 1.f / (__uint_as_float(zq) + (f2_lo(rowsum2) + f2_hi(rowsum2)) + p.eps);
             tc_fence_before();
             fence_proxy_async_smem();
             named_bar_sync(2, 64);
