@@ -194,15 +194,16 @@ __device__ __forceinline__ void state_to_tile_split(uint32_t tacc, uint8_t* tile
     }
 }
 
-// TMEM state -> the caller's [D][DV] array (any alignment), warps 4 .. 4 + D/32 - 1.
+// TMEM state -> the caller's [D][DV] array (any alignment); warps w and w + 4 share lane
+// quarter w % 4 and take one half of the columns each.
 template <int D, int DV>
 __device__ __forceinline__ void state_to_array(uint32_t tacc, float* dst, int warp, int lane) {
-    const int q = warp - 4;
-    if (q < 0 || 32 * q >= D) return;
+    const int q = warp & 3, half = warp >> 2;
+    if (32 * q >= D) return;
     const int i = 32 * q + lane;
     const uint32_t ta = tacc + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1
-    for (int j0 = 0; j0 < DV; j0 += 16) {
+    for (int j0 = half * (DV / 2); j0 < (half + 1) * (DV / 2); j0 += 16) {
         float x[16];
         ld16f(ta + j0, x);
 #pragma unroll
@@ -432,14 +433,13 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         zf[tid] = sum_vec(p.z_in ? p.z_in + (int64_t)bh * D : nullptr, recs + D * DV, p.rec, nbefore, tid);
         rsum[tid] = 0.f;
     }
-    fence_proxy_async_smem();
-    sync_tc();
-    if (!tok && n > 0) {  // the first chunk's operands
+    if (!tok && n > 0) {  // the first chunk's operands, alongside the sums above
         aux_phi_q(0);
         aux_phi_k(0);
-        named_bar_sync(2, 128);
-        aux_zq(0, zf);
     }
+    fence_proxy_async_smem();
+    sync_tc();
+    if (!tok && n > 0) aux_zq(0, zf);
 
     auto off = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
     const uint64_t dVMk = sdesc_sw128(smem_u32(sm + L::VM), 16, 1024);      // [V; M], K-major (K = dv)
@@ -823,12 +823,12 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         dn[act - 64] = dd;
         evs[act - 64] = ee;
     }
-    fence_proxy_async_smem();
-    sync_tc();
-    if (!tok && n > 0) {
+    if (!tok && n > 0) {  // the first chunk's operands, alongside the sums above
         aux_phi_q(0);
         aux_phi_k(0);
     }
+    fence_proxy_async_smem();
+    sync_tc();
 
     auto off = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
     const uint64_t dVk = sdesc_sw128(smem_u32(sm + L::VT), 16, 1024);       // V, K-major (K = dv)
