@@ -28,7 +28,7 @@ EXPORTS = (
     "la_decode_step", "la_causal_bwd", "la_causal_bwd_ex", "la_causal_bwd_workspace_size",
     "la_set_workspace", "la_get_last_device_status",
     "la_get_error_string", "la_last_launch_count", "la_selftest_wait_timeout", "la_checked_build",
-    "la_feature_map_prf", "la_causal_fwd_mapped",
+    "la_feature_map_prf", "la_causal_fwd_mapped", "la_causal_fwd_segments",
 )
 
 
@@ -50,6 +50,8 @@ def _load() -> ctypes.CDLL:
     lib.la_causal_fwd_ex.argtypes = fwd + [i64p, vp, sz, vp]
     lib.la_causal_fwd_mapped.argtypes = fwd + [i64p, vp, sz, vp]
     lib.la_feature_map_prf.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp]
+    lib.la_causal_fwd_segments.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i64, f32, i32,
+                                           vp, sz, vp]
     lib.la_causal_fwd_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32]
     lib.la_causal_fwd_workspace_size.restype = sz
     lib.la_prefill_state.argtypes = fwd + [vp]
@@ -148,6 +150,14 @@ def la_causal_fwd_mapped(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv,
                                   _ptr(z_out), B, H, T, d, dv, chunk, eps, _dtype(dtype, q), _strides(strides),
                                   _ptr(workspace), int(workspace_bytes), _stream(stream, q))
     return _check("la_causal_fwd_mapped", rc)
+
+
+def la_causal_fwd_segments(q, k, v, out, M_in, z_in, M_seg, z_seg, B, H, T, d, dv, seg_len, eps,
+                           dtype=None, workspace=None, workspace_bytes=0, stream=None):
+    rc = lib.la_causal_fwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(M_in), _ptr(z_in), _ptr(M_seg),
+                                    _ptr(z_seg), B, H, T, d, dv, seg_len, eps, _dtype(dtype, q),
+                                    _ptr(workspace), int(workspace_bytes), _stream(stream, q))
+    return _check("la_causal_fwd_segments", rc)
 
 
 def la_feature_map_prf(x, W, out, rows, d, m, dtype=None, stream=None):

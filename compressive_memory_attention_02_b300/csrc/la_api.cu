@@ -250,10 +250,13 @@ static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dt
     return pl;
 }
 
+// With M_seg / z_seg (tensor-core path only, the caller checks): the state after every
+// segment of seg_chunks 64-token chunks is written too.
 static int fwd_impl(const void* q, const void* k, const void* v, void* out, const float* M_in, const float* z_in,
                     float* M_out, float* z_out, int B, int H, int64_t T, int d, int dv, int chunk, float eps,
                     la_dtype dtype, const int64_t* strides, void* ws, size_t ws_bytes, bool use_registered,
-                    cudaStream_t stream, bool phi_ident = false) {
+                    cudaStream_t stream, bool phi_ident = false, float* M_seg = nullptr, float* z_seg = nullptr,
+                    int seg_chunks = 0) {
     t_launches = 0;
     if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || T <= 0 || !(eps >= 0.f)) return LA_ERR_INVALID_ARG;
@@ -321,10 +324,12 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
         fp.ws = pl.nranges > 2 ? wsf : nullptr;
         fp.rec = rec, fp.nranges = pl.nranges, fp.chunks_per_range = pl.chunks_per_range, fp.split = pl.split;
         fp.H = H, fp.T = T, fp.eps = eps, fp.status = ds->status;
+        fp.M_seg = M_seg, fp.z_seg = z_seg, fp.seg_chunks = seg_chunks;
         rc = cuda_rc(launch_fwd_tc(fp, d, dv, B, mq, mk, mv, mo, stream));
         if (!rc) ++t_launches;
         return rc;
     }
+    if (M_seg || z_seg) return LA_ERR_UNSUPPORTED;  // (the caller runs such cases segment by segment)
     if (fwd_simt_smem(d, dv, chunk) > (size_t)kSmemLimit) return LA_ERR_UNSUPPORTED;
     FwdParams p{};
     p.q = q, p.k = k, p.v = v, p.out = out, p.M_in = M_in, p.z_in = z_in, p.M_out = M_out, p.z_out = z_out;
@@ -660,6 +665,59 @@ int la_causal_fwd_mapped(const void* q, const void* k, const void* v, void* out,
                          size_t workspace_bytes, la_stream_t stream) {
     return fwd_impl(q, k, v, out, M_in, z_in, M_out, z_out, B, H, T, d, dv, chunk, eps, dtype, strides, workspace,
                     workspace_bytes, false, (cudaStream_t)stream, true);
+}
+
+static bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+    if (!a || !b) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bn && y < x + an;
+}
+
+int la_causal_fwd_segments(const void* q, const void* k, const void* v, void* out, const float* M_in,
+                           const float* z_in, float* M_seg, float* z_seg, int B, int H, int64_t T, int d, int dv,
+                           int64_t seg_len, float eps, la_dtype dtype, void* workspace, size_t workspace_bytes,
+                           la_stream_t stream) {
+    t_launches = 0;
+    if (!M_seg || !z_seg || B <= 0 || H <= 0 || T <= 0 || seg_len <= 0 || seg_len % 64 != 0)
+        return LA_ERR_INVALID_ARG;
+    if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+    if (!shape_ok(d, dv)) return LA_ERR_UNSUPPORTED;
+    const int64_t BH = (int64_t)B * H, nseg = ceil_div(T, seg_len);
+    const size_t m_bytes = sizeof(float) * (size_t)(BH * d * dv), z_bytes = sizeof(float) * (size_t)(BH * d);
+    // the outputs may overlap neither each other nor the initial state, which every range reads
+    if (overlap(M_seg, m_bytes * nseg, z_seg, z_bytes * nseg) || overlap(M_seg, m_bytes * nseg, M_in, m_bytes) ||
+        overlap(M_seg, m_bytes * nseg, z_in, z_bytes) || overlap(z_seg, z_bytes * nseg, M_in, m_bytes) ||
+        overlap(z_seg, z_bytes * nseg, z_in, z_bytes))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool tc = dtype == LA_BF16 && (d == 64 || d == 128) && (dv == 64 || dv == 128) &&
+                    env_int("LA_FORCE_SIMT", 0) == 0 && T < (int64_t(1) << 31) && aligned16(q) && aligned16(k) &&
+                    aligned16(v) && aligned16(out);
+    if (tc)  // one launch: the state stays on chip across segment boundaries and is written at each
+        return fwd_impl(q, k, v, out, M_in, z_in, nullptr, nullptr, B, H, T, d, dv, 64, eps, dtype, nullptr,
+                        workspace, workspace_bytes, false, s, false, M_seg, z_seg, (int)(seg_len / 64));
+    // other shapes and float32: one call per segment, each starting from the state the previous
+    // one wrote (strided views of the [B,H,T,*] tensors)
+    const size_t es = dtype == LA_BF16 ? 2 : 4;
+    const int64_t st[12] = {(int64_t)H * T * d, T * d, d, (int64_t)H * T * d, T * d, d,
+                            (int64_t)H * T * dv, T * dv, dv, (int64_t)H * T * dv, T * dv, dv};
+    int launches = 0;
+    for (int64_t sg = 0; sg < nseg; ++sg) {
+        const int64_t t0 = sg * seg_len, Ts = std::min<int64_t>(seg_len, T - t0);
+        const float* Mi = sg == 0 ? M_in : M_seg + (sg - 1) * BH * d * dv;
+        const float* zi = sg == 0 ? z_in : z_seg + (sg - 1) * BH * d;
+        const int rc = fwd_impl(static_cast<const char*>(q) + t0 * d * es, static_cast<const char*>(k) + t0 * d * es,
+                                static_cast<const char*>(v) + t0 * dv * es, static_cast<char*>(out) + t0 * dv * es,
+                                Mi, zi, M_seg + sg * BH * d * dv, z_seg + sg * BH * d, B, H, Ts, d, dv, 64, eps,
+                                dtype, st, workspace, workspace_bytes, false, s);
+        launches += t_launches;
+        if (rc) {
+            t_launches = launches;
+            return rc;
+        }
+    }
+    t_launches = launches;
+    return LA_OK;
 }
 
 int la_feature_map_prf(const void* x, const void* W, void* out, int64_t rows, int d, int m, la_dtype dtype,

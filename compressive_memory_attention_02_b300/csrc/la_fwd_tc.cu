@@ -40,6 +40,11 @@
 // Each hand-off is an mbarrier; TMEM reads and writes are ordered with tcgen05 fences
 // around it.
 //
+// Segment-wise output (the SEG variant, la_causal_fwd_segments): after the update of the chunk
+// that ends a segment, the R warps also write the f32 state (M, z) of that segment boundary;
+// the state itself stays in TMEM across the boundary, so a whole segmented sequence is one
+// launch.
+//
 // Sequence split: in the fused two-range schedule (split > 0) range 1 first forms
 // the state of chunks [0, split) itself (phi(K) and the update only) while range 0
 // runs its main pass over the same chunks; in the parts schedule range r adds the
@@ -100,7 +105,9 @@ __device__ __forceinline__ void pack16_bf16(const uint32_t* x, uint32_t* a) {
     for (int k = 0; k < 8; ++k) a[k] = pack_bf16(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1]));
 }
 
-template <int D, int DV>
+// SEG: the state after every segment is written too (compiled separately, so that the
+// other calls run without the bookkeeping)
+template <int D, int DV, bool SEG>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, FwdTcParams p) {
@@ -317,6 +324,52 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             }
             tmem_wait_st();
         };
+        // the f32 state (M^T and z in TMEM) to [D][DV] and [D] arrays (either may be null);
+        // two TMEM loads in flight per wait
+        auto store_state = [&](float* Md, float* zd) {
+            if (L::ZL && zd && zlanes) {  // every lane of the quarter holds all of z
+#pragma unroll 1
+                for (int i0 = 0; i0 < D; i0 += 32) {
+                    uint32_t x[16], y[16];
+                    tmem_ld16(tmem + TM_M + lane_base + i0, x);
+                    tmem_ld16(tmem + TM_M + lane_base + i0 + 16, y);
+                    tmem_wait_ld();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            zd[i0 + e] = __uint_as_float(x[e]);
+                            zd[i0 + 16 + e] = __uint_as_float(y[e]);
+                        }
+                    }
+                }
+            } else if (!L::ZL && zd && has_z) {
+                const uint32_t zb = tmem_ld1(tmem + TM_Z + lane_base);
+                tmem_wait_ld();
+                zd[j] = __uint_as_float(zb);
+            }
+            if (Md && has_row) {
+#pragma unroll 1
+                for (int i0 = 0; i0 < D; i0 += 32) {
+                    uint32_t x[16], y[16];
+                    tmem_ld16(tmem + TM_M + lane_base + i0, x);
+                    tmem_ld16(tmem + TM_M + lane_base + i0 + 16, y);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        Md[(int64_t)(i0 + e) * DV + j] = __uint_as_float(x[e]);
+                        Md[(int64_t)(i0 + 16 + e) * DV + j] = __uint_as_float(y[e]);
+                    }
+                }
+            }
+        };
+        // SEG: the state after the chunk that ends a segment (or the sequence) is written before
+        // the re-cast. The next such chunk and its segment are tracked incrementally (no integer
+        // division on the update -> re-cast path).
+        int seg_next = 0, seg_idx = 0;
+        if constexpr (SEG) {
+            seg_next = (main_begin / p.seg_chunks + 1) * p.seg_chunks - 1;
+            seg_idx = main_begin / p.seg_chunks;
+        }
         bool ok = true;
         int upd = 0;
         const int n_upd = (n_agg > 0 ? 1 : 0) + n_main;
@@ -324,6 +377,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             ok = bar_and(4, 128, mbar_wait(upd_done, upd++ & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
+            if constexpr (SEG) {  // (range 1's state-only chunks: no output)
+                if (n_agg == 0 || u > 0) {
+                    const int c = main_begin + (n_agg > 0 ? u - 1 : u);
+                    if (c == seg_next || c == nch - 1) {
+                        const int64_t sb = (int64_t)seg_idx * gridDim.y + bh;
+                        store_state(p.M_seg ? p.M_seg + sb * D * DV : nullptr, p.z_seg ? p.z_seg + sb * D : nullptr);
+                        seg_next += p.seg_chunks;
+                        ++seg_idx;
+                    }
+                }
+            }
             if (L::ZL && u + 1 < n_upd) {
                 recast();  // z^T rides along in lanes 64-95
                 tc_fence_before();
@@ -345,32 +409,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 named_bar_sync(4, 128);
                 if (ct == 0) mbar_arrive(mt_ready);
             } else if (writes_state) {
-                if (L::ZL && p.z_out && zlanes) {  // every lane of the quarter holds all of z
-#pragma unroll 1
-                    for (int i0 = 0; i0 < D; i0 += 16) {
-                        uint32_t x[16];
-                        tmem_ld16(tmem + TM_M + lane_base + i0, x);
-                        tmem_wait_ld();
-                        if (lane == 0)
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) p.z_out[(int64_t)bh * D + i0 + e] = __uint_as_float(x[e]);
-                    }
-                } else if (!L::ZL && p.z_out && has_z) {
-                    const uint32_t zb = tmem_ld1(tmem + TM_Z + lane_base);
-                    tmem_wait_ld();
-                    p.z_out[(int64_t)bh * D + j] = __uint_as_float(zb);
-                }
-                if (p.M_out && has_row) {
-                    float* dst = p.M_out + (int64_t)bh * D * DV + j;
-#pragma unroll 1
-                    for (int i0 = 0; i0 < D; i0 += 16) {
-                        uint32_t x[16];
-                        tmem_ld16(tmem + TM_M + lane_base + i0, x);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) dst[(int64_t)(i0 + e) * DV] = __uint_as_float(x[e]);
-                    }
-                }
+                store_state(p.M_out ? p.M_out + (int64_t)bh * D * DV : nullptr,
+                            p.z_out ? p.z_out + (int64_t)bh * D : nullptr);
             }
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
@@ -612,12 +652,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     }
 }
 
-template <int D, int DV>
+template <int D, int DV, bool SEG>
 static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
     using L = FwdLayout<D, DV>;
     static_assert(L::ALLOC <= 227 * 1024, "shared memory budget");
-    auto fn = fwd_tc_kernel<D, DV>;
+    auto fn = fwd_tc_kernel<D, DV, SEG>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -635,10 +675,16 @@ static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, 
 
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
-    if (d == 128 && dv == 128) return launch_t<128, 128>(p, B, mq, mk, mv, mo, s);
-    if (d == 128 && dv == 64) return launch_t<128, 64>(p, B, mq, mk, mv, mo, s);
-    if (d == 64 && dv == 128) return launch_t<64, 128>(p, B, mq, mk, mv, mo, s);
-    if (d == 64 && dv == 64) return launch_t<64, 64>(p, B, mq, mk, mv, mo, s);
+    const bool seg = p.M_seg || p.z_seg;
+    if (seg && p.seg_chunks <= 0) return cudaErrorInvalidValue;
+    if (d == 128 && dv == 128) return seg ? launch_t<128, 128, true>(p, B, mq, mk, mv, mo, s)
+                                          : launch_t<128, 128, false>(p, B, mq, mk, mv, mo, s);
+    if (d == 128 && dv == 64) return seg ? launch_t<128, 64, true>(p, B, mq, mk, mv, mo, s)
+                                         : launch_t<128, 64, false>(p, B, mq, mk, mv, mo, s);
+    if (d == 64 && dv == 128) return seg ? launch_t<64, 128, true>(p, B, mq, mk, mv, mo, s)
+                                         : launch_t<64, 128, false>(p, B, mq, mk, mv, mo, s);
+    if (d == 64 && dv == 64) return seg ? launch_t<64, 64, true>(p, B, mq, mk, mv, mo, s)
+                                        : launch_t<64, 64, false>(p, B, mq, mk, mv, mo, s);
     return cudaErrorInvalidValue;
 }
 

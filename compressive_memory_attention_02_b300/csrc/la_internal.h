@@ -139,6 +139,9 @@ struct FwdTcParams {
     float eps;
     int* status;
     int phi_ident;         // q, k hold feature values already (no elu + 1)
+    float* M_seg;          // state after every segment of seg_chunks chunks: [nseg][B*H][d][dv] (or null)
+    float* z_seg;          // [nseg][B*H][d] (or null)
+    int seg_chunks;        // 64-token chunks per segment (> 0 when M_seg or z_seg is set)
 };
 
 // device status word bits

@@ -105,6 +105,29 @@ int la_causal_fwd_ex(const void* q, const void* k, const void* v, void* out,
 size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int chunk,
                                     la_dtype dtype);
 
+/* Segment-wise forward (the "Segment-Wise Attention" page: a sequence split into segments
+ * with the compressive memory M, z carried from each segment to the next), in one call:
+ * the outputs of all T tokens, which are those of la_causal_fwd over the whole sequence
+ * (carrying the state across a segment boundary is the same recurrence step as across a
+ * chunk boundary), and the state after every segment.
+ *   q, k, v, out   contiguous [B,H,T,*] as for la_causal_fwd
+ *   M_in, z_in     state before the first segment, [B,H,d,dv] / [B,H,d] float32; NULL = zero
+ *   M_seg          [nseg][B,H,d,dv] float32, written: M after segment s (nseg = ceil(T / seg_len);
+ *                  the last segment may be shorter, and its entry is the final state)
+ *   z_seg          [nseg][B,H,d] float32, written: z after segment s
+ *   seg_len        tokens per segment, a positive multiple of 64
+ *   workspace      as for la_causal_fwd_ex (enables the sequence-split schedule)
+ * bf16 with d, dv in {64, 128} (16-byte aligned q, k, v, out) runs as one launch of the
+ * chunked kernel, the state staying on chip across segment boundaries and written at each;
+ * other cases run one la_causal_fwd_ex per segment. Errors: LA_ERR_INVALID_ARG for null
+ * M_seg or z_seg, a bad seg_len, or outputs that overlap each other or M_in / z_in; otherwise
+ * as la_causal_fwd_ex. */
+int la_causal_fwd_segments(const void* q, const void* k, const void* v, void* out,
+                           const float* M_in, const float* z_in, float* M_seg, float* z_seg,
+                           int B, int H, int64_t T, int d, int dv, int64_t seg_len, float eps,
+                           la_dtype dtype, void* workspace, size_t workspace_bytes,
+                           la_stream_t stream);
+
 /* ---- other feature maps ------------------------------------------------------
  * The page "Attention_Kernel_Mask" lists positive random features (PRF) and orthogonal
  * random features (ORF) among the feature maps of its non-causal kernel discussion,

@@ -99,3 +99,21 @@ def test_backward_rejects_unaligned_inputs_on_host():
     import compressive_memory_attention_02_b300 as la
     args = [16, 32, 48, 72, None, None, None, None, 80, 96, 112, None, None]  # dout 8 bytes off
     assert la.lib.la_causal_bwd(*args, 1, 1, 64, 64, 64, 1e-6, 1, None) == la.LA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M_seg=None), 1), (dict(z_seg=None), 1), (dict(seg_len=100), 1), (dict(seg_len=0), 1), (dict(T=0), 1),
+    (dict(z_seg=0x10000 + 4096), 1),     # z_seg inside M_seg (2 segments x 64 x 64 floats = 32 KB)
+    (dict(M_in=0x10000 + 8192), 1),      # the initial state inside M_seg
+    (dict(d=7), 2), (dict(dtype=5), 2),
+])
+def test_segments_call_rejects_bad_arguments_on_host(kw, code):
+    """la_causal_fwd_segments checks its arguments before touching the device."""
+    import compressive_memory_attention_02_b300 as la
+    a = dict(q=16, k=32, v=48, out=64, M_in=None, M_seg=0x10000, z_seg=0x40000, B=1, H=1, T=128, d=64, dv=64,
+             seg_len=64, dtype=la.LA_BF16)
+    a.update(kw)
+    rc = la.lib.la_causal_fwd_segments(a["q"], a["k"], a["v"], a["out"], a["M_in"], None, a["M_seg"], a["z_seg"],
+                                       a["B"], a["H"], a["T"], a["d"], a["dv"], a["seg_len"], 1e-6, a["dtype"],
+                                       None, 0, None)
+    assert rc == code

@@ -28,10 +28,11 @@ def _replica(w, rank):
     q, k, v = bench.make_inputs(w, rank)
     M = z = None
     outs = []
-    for s in range(q.shape[0]):
-        o, M, z = oracle.causal_fwd(q[s], k[s], v[s], M_in=M, z_in=z, eps=w.eps)
+    for s in range(w.T // w.segment):
+        sl = slice(s * w.segment, (s + 1) * w.segment)
+        o, M, z = oracle.causal_fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], M_in=M, z_in=z, eps=w.eps)
         outs.append(o)
-    return q, np.stack(outs), M, z
+    return q, np.concatenate(outs, axis=2), M, z
 
 
 def _worker(rank, world, port, queue):
@@ -45,7 +46,7 @@ def _worker(rank, world, port, queue):
         w = _small()
         q, outs, M, z = _replica(w, rank)
         t_max = bench.max_over_ranks(0.5 + rank, dist, "cpu")   # per-rank stand-in times
-        queue.put((rank, bench.replica_seed(w, rank), t_max, q[0, 0, 0, 0, :4].tolist(), float(outs.sum()),
+        queue.put((rank, bench.replica_seed(w, rank), t_max, q[0, 0, 0, :4].tolist(), float(outs.sum()),
                    float(M.sum()), float(z.sum())))
         dist.barrier()
     finally:

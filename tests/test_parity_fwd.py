@@ -8,9 +8,10 @@ import numpy as np
 import pytest
 import torch
 
+import compressive_memory_attention_02_b300 as la
 import oracle
 import synthetic
-from gpu_helpers import TOL_BF16, TOL_F32, fwd, rand_state, to_dev, to_host
+from gpu_helpers import TOL_BF16, TOL_F32, check_status, dtype_code, fwd, rand_state, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -248,3 +249,68 @@ def test_bf16_any_chunk_length_runs_on_the_tensor_core_path(chunk):
     for x, y in zip(a, b):
         assert torch.equal(x, y)
     _compare(a, oracle.causal_fwd(q, k, v), TOL_BF16)
+
+
+# ------------------------------------------------------------------ segment-wise call
+
+def _segments(q, k, v, M0, z0, seg_len, workspace):
+    B, H, T, d = q.shape
+    dv = v.shape[3]
+    nseg = -(-T // seg_len)
+    out = torch.empty(B, H, T, dv, dtype=q.dtype, device="cuda")
+    M_seg = torch.full((nseg, B, H, d, dv), float("nan"), device="cuda")
+    z_seg = torch.full((nseg, B, H, d), float("nan"), device="cuda")
+    nws = la.la_causal_fwd_workspace_size(B, H, T, d, dv, 64, dtype_code(q)) if workspace else 0
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda") if workspace else None
+    la.la_causal_fwd_segments(q, k, v, out, M0, z0, M_seg, z_seg, B, H, T, d, dv, seg_len, 1e-6, dtype_code(q),
+                              ws, nws)
+    n = la.la_last_launch_count()
+    check_status()
+    return out, M_seg, z_seg, n
+
+
+def _segment_refs(q, k, v, M0, z0, seg_len):
+    """The oracle run segment by segment, each segment starting from the state the previous
+    one ended with: every output and the state after each segment."""
+    T = q.shape[2]
+    outs, Ms, zs = [], [], []
+    M, z = M0, z0
+    for t0 in range(0, T, seg_len):
+        sl = slice(t0, min(T, t0 + seg_len))
+        o, M, z = oracle.causal_fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], M_in=M, z_in=z)
+        outs.append(o), Ms.append(M), zs.append(z)
+    return np.concatenate(outs, axis=2), Ms, zs
+
+
+@pytest.mark.parametrize("d,dv,T,seg_len", [(64, 64, 1000, 192), (128, 128, 700, 256), (64, 128, 640, 64),
+                                            (128, 64, 333, 512)])
+@pytest.mark.parametrize("workspace", [False, True])
+def test_bf16_segments_one_launch(d, dv, T, seg_len, workspace):
+    """One launch over all segments (the sequence-split schedules included), the state after
+    every segment written, the last segment ragged."""
+    B, H = 1, 3
+    q, k, v = _inputs(700 + d + dv + T, B, H, T, d, dv, "bf16", 0.5)
+    M0, z0 = rand_state(701, B, H, d, dv)
+    out, M_seg, z_seg, n = _segments(to_dev(q), to_dev(k), to_dev(v), to_dev(M0), to_dev(z0), seg_len, workspace)
+    assert n == (2 if workspace else 1)  # with scratch: the range pre-pass, then the chunked kernel
+    r_out, r_M, r_z = _segment_refs(q, k, v, M0, z0, seg_len)
+    errs = [oracle.rel_err_rows(to_host(out), r_out)]
+    for s in range(len(r_M)):
+        errs.append(oracle.rel_err_state(to_host(M_seg[s]), r_M[s], (2, 3)))
+        errs.append(oracle.rel_err_state(to_host(z_seg[s]), r_z[s], (2,)))
+    print(f"PARITY segments_d{d}_dv{dv}_T{T}_seg{seg_len} max={max(errs):.3e}")
+    assert all(e <= TOL_BF16 for e in errs), errs  # (an entry never written stays NaN and fails)
+
+
+def test_fp32_segments_one_call_per_segment():
+    """float32 (and shapes outside the tensor-core set): one la_causal_fwd_ex per segment."""
+    B, H, T, d, dv, seg_len = 2, 2, 300, 32, 16, 128
+    q, k, v = _inputs(710, B, H, T, d, dv, "f32", 1.0)
+    M0, z0 = rand_state(711, B, H, d, dv)
+    out, M_seg, z_seg, n = _segments(to_dev(q), to_dev(k), to_dev(v), to_dev(M0), to_dev(z0), seg_len, False)
+    assert n == 3
+    r_out, r_M, r_z = _segment_refs(q, k, v, M0, z0, seg_len)
+    assert oracle.rel_err_rows(to_host(out), r_out) <= TOL_F32
+    for s in range(3):
+        assert oracle.rel_err_state(to_host(M_seg[s]), r_M[s], (2, 3)) <= TOL_F32
+        assert oracle.rel_err_state(to_host(z_seg[s]), r_z[s], (2,)) <= TOL_F32
