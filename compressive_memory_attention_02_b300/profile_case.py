@@ -2,9 +2,10 @@
 
   python -m compressive_memory_attention_02_b300.profile_case --mode fwd --B 2 --H 32 --T 2048 --repeat 3
 
-Modes: fwd (la_causal_fwd, training forward), bwd (la_causal_bwd, training
-backward with dout ~ N(0,1)), prefill (la_prefill_state), decode (la_decode_step
-on a [B, H] batch of one-token streams with a random state). Inputs are the seeded synthetic N(0,1)*0.5 bf16 values; the call's
+Modes: fwd (la_causal_fwd, training forward), segments (la_causal_fwd_segments:
+the sequence as segments of --segment tokens, the state written after each), bwd
+(la_causal_bwd, training backward with dout ~ N(0,1)), prefill (la_prefill_state),
+decode (la_decode_step on a [B, H] batch of one-token streams with a random state). Inputs are the seeded synthetic N(0,1)*0.5 bf16 values; the call's
 workspace is registered before the first launch.
 """
 from __future__ import annotations
@@ -20,7 +21,7 @@ if ROOT not in sys.path:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "prefill", "decode"])
+    ap.add_argument("--mode", default="fwd", choices=["fwd", "segments", "bwd", "prefill", "decode"])
     ap.add_argument("--B", type=int, default=2)
     ap.add_argument("--H", type=int, default=32)
     ap.add_argument("--T", type=int, default=2048)
@@ -64,6 +65,16 @@ def main():
             la.ensure_workspace(la.la_causal_fwd_workspace_size(a.B, a.H, a.T, a.d, a.dv, 64, la.LA_BF16))
             for _ in range(a.repeat):
                 la.la_causal_fwd(q, k, v, out, None, None, M, z, a.B, a.H, a.T, a.d, a.dv, 64, 1e-6, la.LA_BF16)
+        elif a.mode == "segments":
+            out = torch.empty(a.B, a.H, a.T, a.dv, dtype=torch.bfloat16, device=dev)
+            nseg = -(-a.T // a.segment)
+            M_seg = torch.empty(nseg, a.B, a.H, a.d, a.dv, device=dev)
+            z_seg = torch.empty(nseg, a.B, a.H, a.d, device=dev)
+            nws = la.la_causal_fwd_workspace_size(a.B, a.H, a.T, a.d, a.dv, 64, la.LA_BF16)
+            ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+            for _ in range(a.repeat):
+                la.la_causal_fwd_segments(q, k, v, out, None, None, M_seg, z_seg, a.B, a.H, a.T, a.d, a.dv,
+                                          a.segment, 1e-6, la.LA_BF16, ws, nws)
         else:
             out = torch.empty(a.B, a.H, a.dv, dtype=torch.bfloat16, device=dev)
             la.ensure_workspace(la.la_prefill_workspace_size(a.B, a.H, a.T, a.d, a.dv, a.segment, la.LA_BF16))
