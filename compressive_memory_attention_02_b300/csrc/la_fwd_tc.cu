@@ -25,9 +25,10 @@
 //
 // One block per (range, head). Warp roles (1024 threads; warp w issues on sub-partition
 // w % 4 and may touch only TMEM lane quarter w % 4):
-//   warp 0        TMA producer: Q, K, V tiles into a 3-stage ring
+//   warp 0        TMA producer: Q, K, V tiles into a 3-stage ring (5 stages at d = dv = 64)
 //   warp 1        TMEM owner; lane 0 issues every tcgen05.mma, software-pipelined one
-//                 chunk ahead: PV_c, then S'_{c+1}, inter_{c+1}, update_{c+1}
+//                 chunk ahead: PV_c, then S'_{c+1}, inter_{c+1}, update_{c+1} (at d = dv = 64,
+//                 where S' does not depend on the state: PV_c, inter_{c+1}, update_{c+1}, S'_{c+2})
 //   warps 2,3,18-20,22-24,26-28,30  F: phi in place on Q and K, zero padded keys (none on
 //                 sub-partition 1, which the MMA-issuing warp uses; warps 21, 25, 29, 31 idle)
 //   warps 4-7     R: after each update, z (bf16) into row 64 of the next chunk's K tile and
@@ -69,7 +70,10 @@ struct FwdLayout {
     // whose A operand is V^T (rows 64-127 of that operand read an atom of ones kept after
     // every V stage), so no key-sum MMA and no z row in the K tile
     static constexpr bool ZL = DV == 64;
-    static constexpr int NST = 3;
+    // d = dv = 64: the scores S' no longer depend on the state (no z row), so the MMA thread
+    // issues them two chunks ahead; a 5-stage ring keeps their operands landed in time
+    static constexpr bool AHEAD = D == 64 && DV == 64;
+    static constexpr int NST = AHEAD ? 5 : 3;
     static constexpr int QB = D / 64 * ATOM;
     static constexpr int KB = D / 64 * ATOMK;
     static constexpr int VB = (ZL ? 2 : DV / 64) * ATOM;
@@ -81,7 +85,7 @@ struct FwdLayout {
     static constexpr int ONES = OT + DV / 64 * ATOM;  // 16 x 64 bf16 ones (2 KB, 1024-aligned)
     static constexpr int RDEN = ONES + 2048;          // 2 x 64 floats
     static constexpr int BAR = RDEN + 2 * 64 * 4;
-    static constexpr int NBAR = 23;
+    static constexpr int NBAR = 3 * NST + 14;
     static constexpr int MISC = BAR + 8 * NBAR;
     static constexpr int TOTAL = MISC + 16;
     static constexpr int ALLOC = TOTAL + 1024;
@@ -117,18 +121,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     uint8_t* sm = align1024(smem_raw);
     float* rden = reinterpret_cast<float*>(sm + L::RDEN);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-    uint64_t* full = bars + 0;      // [3] TMA landed
-    uint64_t* empty = bars + 3;     // [3] stage free (MMA commit)
-    uint64_t* phib = bars + 6;      // [3] phi applied (F)
-    uint64_t* s_full = bars + 9;    // [2] S' ready (MMA commit)
-    uint64_t* s_free = bars + 11;   // [2] S' read (S)
-    uint64_t* p_full = bars + 13;   // [2] P and 1/den written (S)
-    uint64_t* o_full = bars + 15;   // [2] O^T ready (MMA commit)
-    uint64_t* o_free = bars + 17;   // [2] O^T and 1/den read (E)
-    uint64_t* upd_done = bars + 19; // state update finished (MMA commit)
-    uint64_t* mt_ready = bars + 20; // bf16 M^T written and TMEM M read (R)
-    uint64_t* drain = bars + 21;    // all MMAs finished (MMA thread only)
-    uint64_t* zrow_ready = bars + 22; // z before the next main chunk in its K tile's row 64 (E, then R)
+    uint64_t* full = bars + 0;             // [NST] TMA landed
+    uint64_t* empty = bars + NST;          // [NST] stage free (MMA commit)
+    uint64_t* phib = bars + 2 * NST;       // [NST] phi applied (F)
+    uint64_t* s_full = bars + 3 * NST;     // [2] S' ready (MMA commit)
+    uint64_t* s_free = s_full + 2;         // [2] S' read (S)
+    uint64_t* p_full = s_full + 4;         // [2] P and 1/den written (S)
+    uint64_t* o_full = s_full + 6;         // [2] O^T ready (MMA commit)
+    uint64_t* o_free = s_full + 8;         // [2] O^T and 1/den read (E)
+    uint64_t* upd_done = s_full + 10;      // state update finished (MMA commit)
+    uint64_t* mt_ready = s_full + 11;      // bf16 M^T written and TMEM M read (R)
+    uint64_t* drain = s_full + 12;         // all MMAs finished (MMA thread only)
+    uint64_t* zrow_ready = s_full + 13;    // z before the next main chunk in its K tile's row 64 (E, then R)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -251,8 +255,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                         mma_bf16_ss(tmem + TM_Z, kb + off(ks * 2048), d1 + off(ks * 32), id_z, 1);
                 }
             };
-            // S'_m, inter_m, update_m of main chunk m
-            auto front = [&](int m) {
+            // S'_m of main chunk m
+            auto scores = [&](int m) {
                 const int g = n_agg + m, s = g % NST, buf = m & 1;
                 const uint64_t qd = dq0 + off(s * L::QB), kd = dk0 + off(s * L::KB);
                 if (!wait(&phib[s], (g / NST) & 1)) return false;
@@ -264,6 +268,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                     mma_bf16_ss(tmem + tm_s(buf), qd + off((ks >> 2) * ATOM + (ks & 3) * 32),
                                 kd + off((ks >> 2) * ATOMK + (ks & 3) * 32), id_s, ks != 0);
                 mma_commit(&s_full[buf]);
+                return true;
+            };
+            // inter_m and update_m of main chunk m
+            auto state_part = [&](int m) {
+                const int g = n_agg + m, s = g % NST, buf = m & 1;
+                const uint64_t qd = dq0 + off(s * L::QB);
                 if (!wait(mt_ready, mt_waits++ & 1)) return false;
                 if (m >= 2 && !wait(&o_free[buf], ((m >> 1) - 1) & 1)) return false;
                 tc_fence_after();
@@ -275,6 +285,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 mma_commit(upd_done);
                 return true;
             };
+            auto front = [&](int m) { return scores(m) && state_part(m); };
             if (n_agg > 0) {
                 wait(mt_ready, mt_waits++ & 1);  // initial state in TMEM
                 tc_fence_after();
@@ -287,7 +298,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 }
                 if (ok) mma_commit(upd_done);
             }
-            if (ok && n_main > 0) front(0);
+            if constexpr (L::AHEAD) {
+                if (ok && n_main > 0) ok = scores(0) && state_part(0) && (n_main < 2 || scores(1));
+            } else {
+                if (ok && n_main > 0) front(0);
+            }
             for (int m = 0; ok && m < n_main; ++m) {
                 const int g = n_agg + m, s = g % NST, buf = m & 1;
                 if (!wait(&p_full[buf], (m >> 1) & 1)) break;
@@ -298,7 +313,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                                 id_pv, 1);
                 mma_commit(&o_full[buf]);
                 mma_commit(&empty[s]);
-                if (m + 1 < n_main && !front(m + 1)) break;
+                if constexpr (L::AHEAD) {  // the state chain first; the scores two chunks ahead
+                    if (m + 1 < n_main && !state_part(m + 1)) break;
+                    if (m + 2 < n_main && !scores(m + 2)) break;
+                } else {
+                    if (m + 1 < n_main && !front(m + 1)) break;
+                }
             }
             mma_commit(drain);
             mbar_wait_drain(drain, 0);
