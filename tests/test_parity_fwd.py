@@ -314,3 +314,48 @@ def test_fp32_segments_one_call_per_segment():
     for s in range(3):
         assert oracle.rel_err_state(to_host(M_seg[s]), r_M[s], (2, 3)) <= TOL_F32
         assert oracle.rel_err_state(to_host(z_seg[s]), r_z[s], (2,)) <= TOL_F32
+
+
+def test_bf16_segments_outside_the_tensor_core_shapes():
+    """bf16 with d, dv outside {64, 128}: one la_causal_fwd_ex per segment (SIMT kernel)."""
+    B, H, T, d, dv, seg_len = 1, 2, 200, 32, 16, 64
+    q, k, v = _inputs(720, B, H, T, d, dv, "bf16", 0.5)
+    M0, z0 = rand_state(721, B, H, d, dv)
+    out, M_seg, z_seg, n = _segments(to_dev(q), to_dev(k), to_dev(v), to_dev(M0), to_dev(z0), seg_len, False)
+    assert n == 4
+    r_out, r_M, r_z = _segment_refs(q, k, v, M0, z0, seg_len)
+    errs = [oracle.rel_err_rows(to_host(out), r_out)]
+    for s in range(4):
+        errs.append(oracle.rel_err_state(to_host(M_seg[s]), r_M[s], (2, 3)))
+        errs.append(oracle.rel_err_state(to_host(z_seg[s]), r_z[s], (2,)))
+    assert all(e <= TOL_BF16 for e in errs), errs
+
+
+def test_bf16_segments_in_a_cuda_graph_equal_eager_calls():
+    """The one-launch segments call captured in a CUDA graph gives the eager call's bits."""
+    B, H, T, d, seg_len = 2, 4, 1024, 128, 256
+    q, k, v = (to_dev(a) for a in _inputs(730, B, H, T, d, d, "bf16", 0.5))
+    outs = []
+    for graph in (False, True):
+        out = torch.empty(B, H, T, d, dtype=torch.bfloat16, device="cuda")
+        M_seg = torch.empty(T // seg_len, B, H, d, d, device="cuda")
+        z_seg = torch.empty(T // seg_len, B, H, d, device="cuda")
+        call = lambda: la.la_causal_fwd_segments(q, k, v, out, None, None, M_seg, z_seg, B, H, T, d, d, seg_len,
+                                                 1e-6, la.LA_BF16)
+        if graph:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                call()  # attributes set and modules loaded outside the capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                call()
+            out.zero_(), M_seg.zero_(), z_seg.zero_()
+            g.replay()
+        else:
+            call()
+        torch.cuda.synchronize()
+        check_status()
+        outs.append((out.clone(), M_seg.clone(), z_seg.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
