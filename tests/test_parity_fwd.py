@@ -200,6 +200,41 @@ def test_segmented_workload_full_sampled_heads():
     assert bool((out.float().abs() <= vmax * 1.02 + 1e-6).all())
 
 
+def test_segments_call_full_workload_sampled_heads():
+    """The segmented workload as the bench runs it: one la_causal_fwd_segments call over
+    B=2, H=32, T=32768 (16 segments of 2048, the bench's workspace), checked on sampled heads
+    against the oracle run segment by segment: all 32768 outputs and the state after every
+    segment."""
+    w = synthetic.WORKLOADS["segmented"]
+    q, k, v = synthetic.qkv(w)
+    B, H, T, d, dv, S = w.B, w.H, w.T, w.d, w.dv, w.segment
+    nseg = T // S
+    out = torch.empty(B, H, T, dv, dtype=torch.bfloat16, device="cuda")
+    M_seg = torch.full((nseg, B, H, d, dv), float("nan"), device="cuda")
+    z_seg = torch.full((nseg, B, H, d), float("nan"), device="cuda")
+    nws = la.la_causal_fwd_workspace_size(B, H, T, d, dv, w.chunk, la.LA_BF16)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    la.la_causal_fwd_segments(to_dev(q), to_dev(k), to_dev(v), out, None, None, M_seg, z_seg, B, H, T, d, dv, S,
+                              w.eps, la.LA_BF16, ws, nws)
+    assert la.la_last_launch_count() == 1
+    check_status()
+    heads = [(0, 0), (0, 31), (1, 7), (1, 20)]
+    sel = lambda a: np.stack([a[b, h] for b, h in heads])[None]
+    r_out, r_M, r_z = _segment_refs(sel(q), sel(k), sel(v), None, None, S)
+    errs = {"out": oracle.rel_err_rows(np.stack([to_host(out[b, h]) for b, h in heads])[None], r_out)}
+    for s in range(nseg):
+        g_M = np.stack([to_host(M_seg[s, b, h]) for b, h in heads])[None]
+        g_z = np.stack([to_host(z_seg[s, b, h]) for b, h in heads])[None]
+        errs[f"M{s}"] = oracle.rel_err_state(g_M, r_M[s], (2, 3))
+        errs[f"z{s}"] = oracle.rel_err_state(g_z, r_z[s], (2,))
+    worst = max(errs, key=lambda key: errs[key])
+    print(f"PARITY workload_segments_call out={errs['out']:.3e} worst={worst}:{errs[worst]:.3e} "
+          f"(4 sampled heads, 32768 tokens, 16 segment states)")
+    assert all(e <= TOL_BF16 for e in errs.values()), errs
+    # every head and segment state was written (no NaN left), and the last segment's is finite
+    assert not bool(torch.isnan(M_seg).any()) and not bool(torch.isnan(z_seg).any())
+
+
 def test_bf16_calls_captured_in_a_cuda_graph_match_eager_calls():
     """Segment calls chained through M, z, captured in one CUDA graph and replayed, give the
     eager calls' results bit for bit (the calls make no synchronising CUDA call)."""
