@@ -26,11 +26,12 @@
 // order in its prologue and range 0 of the second sweep ends with the gradient of the
 // initial state; with more, the ordered scans of la_bwd.cu do it between the launches.
 //
-// G and dA are formed in f32 and enter their products as two bf16 operands, the high part
-// and the rounded remainder (x = hi + lo to ~16 bits), so that the cancellations in dq
-// (M g + e z against the intra-chunk sum, and g . v_j + e inside dA) act on f32-accurate
-// values. phi, V, dout, the carried states and P enter as bf16 (P reaches dv alone, whose
-// sums do not cancel the way dq's do).
+// G and dA are formed in f32 and enter the dq sweep's products as two bf16 operands, the
+// high part and the rounded remainder (x = hi + lo to ~16 bits), so that the cancellations
+// in dq (M g + e z against the intra-chunk sum, and g . v_j + e inside dA) act on
+// f32-accurate values. In the dk/dv sweep G stays split where it forms dA^T and sums into the
+// state gradient R; dv's P^T G and dk's dA^T phi(Q) take the high parts alone. phi, V, dout,
+// the carried states and P enter as bf16.
 //
 // 256 threads; warp w may touch only TMEM lane quarter w % 4. Per-token passes use warps 0
 // and 1 (lanes 0-63 = the chunk's tokens), state copies warps 4-7. Thread 0 issues the TMA
@@ -708,7 +709,7 @@ struct DkvLayout {
 // Chunk steps of the dk/dv sweep (chunks in reverse; roles as in the dq sweep):
 //   start   wait Q, K (phi already applied), dout; G = dout / D (hi, lo), column halves
 //   g1      S^T = phi(K) phi(Q)^T, [dA^T | V R^T] = V [G; R]^T, R += phi(Q)^T G
-//   mask    P^T, dA^T + e masked to queries at or after the key (hi, lo) | aux: phi(Q) next
+//   mask    P^T, dA^T + e masked to queries at or after the key (bf16)  | aux: phi(Q) next
 //   g2      dv = P^T G + phi(K) R, dphi(K) += dA^T phi(Q)      | aux: phi(K) next, r
 //   end     dk = (dphi(K) + r) phi'(k), dv; R to its bf16 tile
 template <int D, int DV>
@@ -919,7 +920,7 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         ++mph, ++pend[B_MMA].waited;
         tc_fence_after();
         if (tid == 0 && more) load_v(idx + 1);  // V's only reader (g1) is done
-        // ---- mask: P^T (bf16: it enters dv alone) and dA^T + e (high and low parts), masked to
+        // ---- mask: P^T and dA^T + e (bf16: each enters one product of the high parts), masked to
         // queries at or after the key; key rows, query-column halves
         if (tok) {
             const int j = trow, hf = thalf;
@@ -929,18 +930,17 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
             ld32f(tmem + L::TA + lb + 32 * hf, a);
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
-                uint32_t ph[8], ah[8], al[8];
+                uint32_t ph[8], ah[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const int c = 16 * g + 2 * q, tq = 32 * hf + c;
                     const bool m0 = tq >= j, m1 = tq + 1 >= j;
                     ph[q] = pack_bf16(m0 ? sv[c] : 0.f, m1 ? sv[c + 1] : 0.f);
-                    split2(m0 ? a[c] + ec[tq] : 0.f, m1 ? a[c + 1] + ec[tq + 1] : 0.f, ah[q], al[q]);
+                    ah[q] = pack_bf16(m0 ? a[c] + ec[tq] : 0.f, m1 ? a[c + 1] + ec[tq + 1] : 0.f);
                 }
                 const int col = 32 * hf + 16 * g;
                 tile_put16(sm + L::PT, j, col, ATOM, ph);
                 tile_put16(sm + L::AT, j, col, ATOM, ah);
-                tile_put16(sm + L::AT + ATOM, j, col, ATOM, al);
             }
             fence_proxy_async_smem();
         } else if (more) {
@@ -953,11 +953,10 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
             constexpr uint32_t id_kq = idesc_bf16(128, D, 0, 1);
 #pragma unroll
             for (int ks = 0; ks < CH / 16; ++ks) {
-                // P^T G with G split: P^T G_hi + P^T G_lo
+                // dv's P^T G and dk's dA^T phi(Q) on the high parts alone; the state gradient R,
+                // which sums over the whole range, keeps G's low part
                 mma_bf16_ss(tmem + L::TS, dPk + off(ks * 32), dGHm + off(ks * 2048), id_vg, ks != 0);
-                mma_bf16_ss(tmem + L::TS, dPk + off(ks * 32), dGLm + off(ks * 2048), id_vg, 1);
                 mma_bf16_ss(tmem + L::TK, dAk + off(ks * 32), dQm + off(ks * 2048), id_kq, 1);
-                mma_bf16_ss(tmem + L::TK, dAk + off(ATOM + ks * 32), dQm + off(ks * 2048), id_kq, 1);
             }
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)

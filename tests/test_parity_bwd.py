@@ -174,3 +174,23 @@ def test_bf16_sweeps_partial_state_arguments(monkeypatch, cpr, grads):
     else:
         ref[4] = None
     _compare(got, tuple(ref), TOL_BF16, f"partial_{grads}_cpr{cpr}")
+
+
+def test_bf16_training_workload_full_sampled_heads():
+    """The training backward at the size the bench times (B=4, H=16, T=4096, d=dv=64, dout ~
+    N(0,1)), one call over every head, checked on sampled heads against the oracle backward
+    (each head's gradients depend on that head's inputs alone)."""
+    w = synthetic.WORKLOADS["train"]
+    B, H, T, d, dv = w.B, w.H, w.T, w.d, w.dv
+    q, k, v = synthetic.qkv(w)
+    dout = synthetic.normal(w.seed, 7, (B, H, T, dv), 1.0, "bf16")
+    got = bwd(to_dev(q), to_dev(k), to_dev(v), to_dev(dout))
+    heads = [(0, 0), (1, 9), (3, 15)]
+    sel = lambda a: np.stack([a[b, h] for b, h in heads])[None]
+    ref = oracle.causal_bwd(sel(q), sel(k), sel(v), _values(sel(dout)))
+    got_sel = tuple(np.stack([to_host(g[b, h]) for b, h in heads])[None] for g in got)
+    errs = {}
+    for key, g, r in zip(("dq", "dk", "dv", "dM_in", "dz_in"), got_sel, ref):
+        errs[key] = oracle.rel_err_state(g, r, tuple(range(2, r.ndim)))
+    print("PARITY bwd_training_workload " + " ".join(f"{k}={v:.3e}" for k, v in errs.items()))
+    assert max(errs.values()) <= TOL_BF16, errs
