@@ -203,8 +203,15 @@ struct FwdPlan {
     int nranges = 1;
     int chunks_per_range = 0;
     int split = 0;
+    int meet = -1;            // fused2 with a hand-off: range 0 publishes its state after this chunk
     size_t ws_bytes = 0;      // scratch that enables the plan (0: none needed)
 };
+
+// Scratch of the fused schedule's hand-off: one state record per head, then one word per head.
+static size_t pub_bytes(int64_t BH, int d, int dv) {
+    const size_t rec = sizeof(float) * ((size_t)d * dv + d) * (size_t)BH;
+    return ((rec + 255) / 256) * 256 + ((sizeof(int) * (size_t)BH + 255) / 256) * 256;
+}
 
 static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dtype dtype, int sm_count,
                         bool aliased, size_t ws_avail) {
@@ -239,14 +246,32 @@ static FwdPlan plan_fwd(int B, int H, int64_t T, int d, int dv, int chunk, la_dt
         P = 2;
     }
     if (ws_avail < alias_bytes) return pl;
+    pl.nranges = 2;
+    pl.ws_bytes = alias_bytes;
+    // With scratch for the hand-off, range 0 publishes its state after chunk meet and range 1
+    // sums only the chunks between meet and the split: range 0 takes a smaller share.
+    const size_t pubb = pub_bytes(BH, d, dv);
+    // (a cooperative grid cannot start its set-up under the previous kernel, and the hand-off
+    // itself costs a few microseconds: it pays only on long sequences)
+    const int64_t min_chunks = env_int("LA_FWD_PUB_MIN_CHUNKS", 256);
+    if (env_int("LA_FWD_PUBLISH", 1) && nch >= min_chunks && ws_avail >= alias_bytes + pubb) {
+        const int pct = env_int("LA_FWD_SPLIT_PCT", d >= 128 ? 60 : 60);
+        const int meet_pct = env_int("LA_FWD_MEET_PCT", 33);  // of the split
+        int64_t split = (nch * pct + 50) / 100;
+        split = std::max<int64_t>(3, std::min<int64_t>(split, nch - 1));
+        int64_t meet = (split * meet_pct + 50) / 100 - 1;
+        meet = std::max<int64_t>(0, std::min<int64_t>(meet, split - 2));  // range 1 sums at least one chunk
+        pl.split = (int)split;
+        pl.meet = (int)meet;
+        pl.ws_bytes = alias_bytes + pubb;
+        return pl;
+    }
     // range 0's share of the chunks: range 1 re-forms their state first (measured optimum:
     // 68% at d = 128, 66% at d = 64, where a chunk's fixed costs weigh more)
     const int pct = env_int("LA_FWD_SPLIT_PCT", d >= 128 ? 68 : 66);
     int64_t split = (nch * pct + 50) / 100;
     split = std::max<int64_t>(1, std::min<int64_t>(split, nch - 1));
-    pl.nranges = 2;
     pl.split = (int)split;
-    pl.ws_bytes = alias_bytes;
     return pl;
 }
 
@@ -325,6 +350,13 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
         fp.rec = rec, fp.nranges = pl.nranges, fp.chunks_per_range = pl.chunks_per_range, fp.split = pl.split;
         fp.H = H, fp.T = T, fp.eps = eps, fp.status = ds->status;
         fp.M_seg = M_seg, fp.z_seg = z_seg, fp.seg_chunks = seg_chunks;
+        if (pl.meet >= 0) {  // the hand-off area follows the aliased-state copy, if any
+            const size_t alias_floats = aliased ? (size_t)BH * rec : 0;
+            fp.pub = wsf + alias_floats;
+            fp.pub_flag = reinterpret_cast<int*>(reinterpret_cast<char*>(fp.pub) +
+                                                 ((sizeof(float) * (size_t)BH * rec + 255) / 256) * 256);
+            fp.meet = pl.meet;
+        }
         rc = cuda_rc(launch_fwd_tc(fp, d, dv, B, mq, mk, mv, mo, stream));
         if (!rc) ++t_launches;
         return rc;

@@ -48,8 +48,12 @@
 //
 // Sequence split: in the fused two-range schedule (split > 0) range 1 first forms
 // the state of chunks [0, split) itself (phi(K) and the update only) while range 0
-// runs its main pass over the same chunks; in the parts schedule range r adds the
-// aggregates of ranges < r written by parts_tc.
+// runs its main pass over the same chunks. With a hand-off area (pub), range 0 writes its
+// state after chunk `meet` to it and range 1 forms only the sum of chunks meet+1 .. split-1,
+// then adds the published state (a word per head: armed by range 1 at its start, set by
+// range 0 once the state is written, cleared by range 1 after reading it; every wait on it
+// is bounded, and the grid is launched cooperatively so that both ranges are resident). In
+// the parts schedule range r adds the aggregates of ranges < r written by parts_tc.
 //
 // Operand layouts (128-byte swizzle, 1024-byte aligned atoms, 16-byte chunk c of row
 // r at chunk c ^ (r % 8)): Q, K, V tiles as TMA loads them ([64 tokens][64 features]
@@ -98,6 +102,29 @@ __device__ __forceinline__ uint32_t tm_s(int buf) { return 192u + 80u * buf; }  
 __device__ __forceinline__ uint32_t tm_o(int buf) { return 352u + 64u * buf; }  // O^T, 64 columns each
 constexpr uint32_t TM_Z = 480;   // z f32, lane = feature, 16 equal columns
 
+// Hand-off words of the fused schedule's state hand-off (arbitrary tags, so that a stale or
+// uninitialised word is never taken for either)
+constexpr int PUB_ARMED = 0x4C410001;
+constexpr int PUB_DONE = 0x4C410002;
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait for a hand-off word written by another block of the same (cooperative) grid.
+__device__ __forceinline__ bool wait_word(const int* p, int want, volatile int* abort_flag) {
+    const unsigned long long t0 = clock64();
+    while (ld_acquire_gpu(p) != want) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > LA_WAIT_CYCLES) return false;
+    }
+    return true;
+}
+
 // bf16 z_i into row 64 (a multiple of 8: no swizzle offset) of a K tile with atoms ATOMK apart
 __device__ __forceinline__ void put_zrow(uint8_t* ktile, int i, float z) {
     *reinterpret_cast<__nv_bfloat16*>(ktile + (i >> 6) * ATOMK + 64 * 128 + (i & 63) * 2) = __float2bfloat16_rn(z);
@@ -109,9 +136,9 @@ __device__ __forceinline__ void pack16_bf16(const uint32_t* x, uint32_t* a) {
     for (int k = 0; k < 8; ++k) a[k] = pack_bf16(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1]));
 }
 
-// SEG: the state after every segment is written too (compiled separately, so that the
-// other calls run without the bookkeeping)
-template <int D, int DV, bool SEG>
+// SEG: the state after every segment is written too; PUB: the fused schedule's state hand-off
+// (each compiled separately, so that the other calls run without the bookkeeping)
+template <int D, int DV, bool SEG, bool PUB>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, FwdTcParams p) {
@@ -140,11 +167,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     const int r = blockIdx.x, bh = blockIdx.y;
     const int b = bh / p.H, h = bh % p.H;
     const int nch = (int)((p.T + CH - 1) / CH);
-    int main_begin, main_end, n_agg = 0, nws = 0;
+    // Fused schedule with a hand-off (pub set): range 0 publishes its state after chunk meet,
+    // and range 1 sums only chunks meet+1 .. split-1 before adding it (blocks co-resident: the
+    // grid is launched cooperatively).
+    const bool publish = PUB && p.split > 0;
+    int main_begin, main_end, n_agg = 0, nws = 0, agg_begin = 0;
     if (p.split > 0) {
         main_begin = r == 0 ? 0 : p.split;
         main_end = r == 0 ? p.split : nch;
-        n_agg = r == 0 ? 0 : p.split;
+        n_agg = r == 0 ? 0 : (publish ? p.split - p.meet - 1 : p.split);
+        agg_begin = publish ? p.meet + 1 : 0;
     } else {
         main_begin = r * p.chunks_per_range;
         main_end = min(nch, main_begin + p.chunks_per_range);
@@ -189,6 +221,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     // before it has completed. This block lets the next such launch start its own set-up.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
+    if (publish && r == 1 && threadIdx.x == 0) atomicExch(&p.pub_flag[bh], PUB_ARMED);
 
     if (warp == 0) {
         // ======================================================== TMA producer
@@ -202,7 +235,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                     break;
                 }
                 const bool is_main = g >= n_agg;
-                const int t = (is_main ? main_begin + g - n_agg : g) * CH;
+                const int t = (is_main ? main_begin + g - n_agg : agg_begin + g) * CH;
                 mbar_expect_tx(&full[s], ((is_main ? D : 0) + D + DV) * CH * 2);
 #pragma unroll
                 for (int a = 0; a < D / 64; ++a) {
@@ -382,6 +415,37 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 }
             }
         };
+        // the f32 state of another block ([D][DV] and [D], read through L2) added into TMEM
+        auto add_state = [&](const float* Mp, const float* zp) {
+            if (has_row) {
+#pragma unroll 1
+                for (int i0 = 0; i0 < D; i0 += 16) {
+                    uint32_t x[16];
+                    tmem_ld16(tmem + TM_M + lane_base + i0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        x[e] = __float_as_uint(__uint_as_float(x[e]) + __ldcg(Mp + (int64_t)(i0 + e) * DV + j));
+                    tmem_st16(tmem + TM_M + lane_base + i0, x);
+                }
+            }
+            if (L::ZL && zlanes) {  // z^T in every lane of the quarter
+#pragma unroll 1
+                for (int i0 = 0; i0 < D; i0 += 16) {
+                    uint32_t x[16];
+                    tmem_ld16(tmem + TM_M + lane_base + i0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) + __ldcg(zp + i0 + e));
+                    tmem_st16(tmem + TM_M + lane_base + i0, x);
+                }
+            } else if (!L::ZL && has_z) {
+                const uint32_t zb = tmem_ld1(tmem + TM_Z + lane_base);
+                tmem_wait_ld();
+                tmem_st1(tmem + TM_Z + lane_base, __float_as_uint(__uint_as_float(zb) + __ldcg(zp + j)));
+            }
+            tmem_wait_st();
+        };
         // SEG: the state after the chunk that ends a segment (or the sequence) is written before
         // the re-cast. The next such chunk and its segment are tracked incrementally (no integer
         // division on the update -> re-cast path).
@@ -397,6 +461,28 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             ok = bar_and(4, 128, mbar_wait(upd_done, upd++ & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
+            if (publish && r == 1 && u == 0) {
+                // range 1, its sum of chunks meet+1 .. split-1 done: add range 0's state after
+                // chunk meet, then clear the hand-off word for the next call (which re-arms it)
+                bool got = true;
+                if (ct == 0) {
+                    got = wait_word(p.pub_flag + bh, PUB_DONE, abort_flag);
+                    if (!got) record_timeout(p.status, abort_flag);
+                }
+                ok = bar_and(4, 128, got);
+                if (!ok) break;
+                const float* pm = p.pub + (int64_t)bh * p.rec;
+                add_state(pm, pm + D * DV);
+                named_bar_sync(4, 128);
+                if (ct == 0) atomicExch(p.pub_flag + bh, 0);
+            }
+            // range 0: its state after chunk meet, published once the re-cast below is done
+            const bool pub_here = publish && r == 0 && u == p.meet;
+            if (pub_here) {
+                float* pm = p.pub + (int64_t)bh * p.rec;
+                store_state(pm, pm + D * DV);
+                __threadfence();
+            }
             if constexpr (SEG) {  // (range 1's state-only chunks: no output)
                 if (n_agg == 0 || u > 0) {
                     const int c = main_begin + (n_agg > 0 ? u - 1 : u);
@@ -432,6 +518,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 store_state(p.M_out ? p.M_out + (int64_t)bh * D * DV : nullptr,
                             p.z_out ? p.z_out + (int64_t)bh * D : nullptr);
             }
+            // (the branch above ended with a barrier of the R warps, after every thread's fence;
+            // range 1 armed the word at its start)
+            if (pub_here && ct == 0) {
+                __threadfence();
+                if (wait_word(p.pub_flag + bh, PUB_ARMED, abort_flag))
+                    st_release_gpu(p.pub_flag + bh, PUB_DONE);
+                else
+                    record_timeout(p.status, abort_flag);
+            }
         }
         if (!ok && ct == 0) record_timeout(p.status, abort_flag);
     } else if (warp >= 8 && warp < 16) {
@@ -444,7 +539,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         const bool has_row = 32 * q < DV;         // warp-uniform
         if (has_row) {
             // column j of the initial state M_in (+ range aggregates), rows [64hf, 64hf + 64)
-            const float* src = p.M_in ? p.M_in + (int64_t)bh * D * DV + j : nullptr;
+            // (range 1 with a hand-off starts from zero: range 0's published state holds M_in)
+            const float* src = p.M_in && !(publish && r == 1) ? p.M_in + (int64_t)bh * D * DV + j : nullptr;
 #pragma unroll 1
             for (int i0 = 64 * hf; i0 < D && i0 < 64 * hf + 64; i0 += 16) {
                 uint32_t x[16], a[8];
@@ -475,7 +571,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 uint32_t x[16], a[8];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    float zz = p.z_in ? p.z_in[(int64_t)bh * D + i0 + e] : 0.f;
+                    float zz = p.z_in && !(publish && r == 1) ? p.z_in[(int64_t)bh * D + i0 + e] : 0.f;
                     for (int pp = 0; pp < nws; ++pp) zz += agg[pp * p.rec + D * DV + i0 + e];
                     x[e] = __float_as_uint(zz);
                 }
@@ -488,7 +584,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         if (!L::ZL && hf == 0 && 32 * q < D) {
             // z_in (+ range aggregates) into TMEM; with no state-only chunks before the first
             // main chunk it is also z before that chunk (row 64 of its K tile, stage 0)
-            float zz = p.z_in ? p.z_in[(int64_t)bh * D + j] : 0.f;
+            float zz = p.z_in && !(publish && r == 1) ? p.z_in[(int64_t)bh * D + j] : 0.f;
             for (int pp = 0; pp < nws; ++pp) zz += agg[pp * p.rec + D * DV + j];
             tmem_st1(tmem + TM_Z + lane_base, __float_as_uint(zz));
             tmem_wait_st();
@@ -653,7 +749,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             const bool is_main = g >= n_agg;
             ok = bar_and(1, 32 * NFW, mbar_wait(&full[s], (g / NST) & 1, abort_flag));
             if (!ok) break;
-            const int64_t t0 = (int64_t)(is_main ? main_begin + g - n_agg : g) * CH;
+            const int64_t t0 = (int64_t)(is_main ? main_begin + g - n_agg : agg_begin + g) * CH;
             const int valid = (int)min64(CH, p.T - t0);
             if (is_main) phi_tile<D, 32 * NFW>(sm + L::Q0 + s * L::QB, ATOM, CH, ct, nullptr, p.phi_ident);
             phi_tile<D, 32 * NFW>(sm + L::K0 + s * L::KB, ATOMK, valid, ct, nullptr, p.phi_ident);
@@ -672,12 +768,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     }
 }
 
-template <int D, int DV, bool SEG>
+template <int D, int DV, bool SEG, bool PUB>
 static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
     using L = FwdLayout<D, DV>;
     static_assert(L::ALLOC <= 227 * 1024, "shared memory budget");
-    auto fn = fwd_tc_kernel<D, DV, SEG>;
+    auto fn = fwd_tc_kernel<D, DV, SEG, PUB>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -685,26 +781,35 @@ static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, 
     cfg.blockDim = dim3(FWD_THREADS);
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // the state hand-off between the two ranges of a head needs every block resident at once
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = PUB ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, fn, mq, mk, mv, mo, p);
 }
 
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
     const bool seg = p.M_seg || p.z_seg;
+    const bool pub = p.pub != nullptr && p.split > 0;
     if (seg && p.seg_chunks <= 0) return cudaErrorInvalidValue;
-    if (d == 128 && dv == 128) return seg ? launch_t<128, 128, true>(p, B, mq, mk, mv, mo, s)
-                                          : launch_t<128, 128, false>(p, B, mq, mk, mv, mo, s);
-    if (d == 128 && dv == 64) return seg ? launch_t<128, 64, true>(p, B, mq, mk, mv, mo, s)
-                                         : launch_t<128, 64, false>(p, B, mq, mk, mv, mo, s);
-    if (d == 64 && dv == 128) return seg ? launch_t<64, 128, true>(p, B, mq, mk, mv, mo, s)
-                                         : launch_t<64, 128, false>(p, B, mq, mk, mv, mo, s);
-    if (d == 64 && dv == 64) return seg ? launch_t<64, 64, true>(p, B, mq, mk, mv, mo, s)
-                                        : launch_t<64, 64, false>(p, B, mq, mk, mv, mo, s);
+    if (pub && (!p.pub_flag || p.meet < 0 || p.meet > p.split - 2)) return cudaErrorInvalidValue;
+#define LA_FWD_SHAPE(DD, DDV)                                                                         \
+    if (d == DD && dv == DDV) {                                                                       \
+        if (seg) return pub ? launch_t<DD, DDV, true, true>(p, B, mq, mk, mv, mo, s)                  \
+                            : launch_t<DD, DDV, true, false>(p, B, mq, mk, mv, mo, s);                \
+        return pub ? launch_t<DD, DDV, false, true>(p, B, mq, mk, mv, mo, s)                          \
+                   : launch_t<DD, DDV, false, false>(p, B, mq, mk, mv, mo, s);                        \
+    }
+    LA_FWD_SHAPE(128, 128)
+    LA_FWD_SHAPE(128, 64)
+    LA_FWD_SHAPE(64, 128)
+    LA_FWD_SHAPE(64, 64)
+#undef LA_FWD_SHAPE
     return cudaErrorInvalidValue;
 }
 

@@ -139,6 +139,10 @@ struct FwdTcParams {
     float eps;
     int* status;
     int phi_ident;         // q, k hold feature values already (no elu + 1)
+    float* pub;            // fused schedule with a hand-off (or null): range 0's state after chunk
+                           // `meet`, [B*H][rec] (M at +0, z at +d*dv), read by range 1
+    int* pub_flag;         // [B*H] hand-off words: armed by range 1, published by range 0
+    int meet;              // range 1 sums chunks meet+1 .. split-1 and adds range 0's state after meet
     float* M_seg;          // state after every segment of seg_chunks chunks: [nseg][B*H][d][dv] (or null)
     float* z_seg;          // [nseg][B*H][d] (or null)
     int seg_chunks;        // 64-token chunks per segment (> 0 when M_seg or z_seg is set)

@@ -394,3 +394,30 @@ def test_bf16_segments_in_a_cuda_graph_equal_eager_calls():
         outs.append((out.clone(), M_seg.clone(), z_seg.clone()))
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("T", [200, 1000])
+def test_bf16_fused_state_hand_off(monkeypatch, d, dv, T):
+    """The fused two-range schedule with range 0 handing its state after chunk `meet` to range
+    1 (forced on short sequences): outputs and final state with an initial state, twice in a row
+    (the second call re-arms the hand-off word the first cleared), and through the segments call."""
+    monkeypatch.setenv("LA_FWD_PUB_MIN_CHUNKS", "1")
+    monkeypatch.setenv("LA_FWD_RANGES", "2")  # the two-range schedule (few heads would take the parts one)
+    B, H = 1, 3
+    q, k, v = _inputs(740 + d + dv + T, B, H, T, d, dv, "bf16", 0.5)
+    M0, z0 = rand_state(741, B, H, d, dv)
+    ref = oracle.causal_fwd(q, k, v, M_in=M0, z_in=z0)
+    for _ in range(2):
+        got = fwd(to_dev(q), to_dev(k), to_dev(v), to_dev(M0), to_dev(z0))
+        check_status()
+        _compare(got, ref, TOL_BF16)
+    out, M_seg, z_seg, n = _segments(to_dev(q), to_dev(k), to_dev(v), to_dev(M0), to_dev(z0), 128, True)
+    assert n == 1
+    r_out, r_M, r_z = _segment_refs(q, k, v, M0, z0, 128)
+    errs = [oracle.rel_err_rows(to_host(out), r_out)]
+    for s in range(len(r_M)):
+        errs.append(oracle.rel_err_state(to_host(M_seg[s]), r_M[s], (2, 3)))
+        errs.append(oracle.rel_err_state(to_host(z_seg[s]), r_z[s], (2,)))
+    print(f"PARITY hand_off_d{d}_dv{dv}_T{T} max={max(errs):.3e}")
+    assert all(e <= TOL_BF16 for e in errs), errs
