@@ -777,8 +777,12 @@ size_t la_causal_fwd_workspace_size(int B, int H, int64_t T, int d, int dv, int 
     int sm = 148;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
-    // the largest scratch any plan for this shape may use (an in-place state included)
-    return plan_fwd(B, H, T, d, dv, chunk, dtype, sm, true, SIZE_MAX).ws_bytes;
+    // the largest scratch any plan for this shape may use (an in-place state included); a
+    // two-range plan counts the state hand-off of long sequences at every T, so that the
+    // size does not depend on T
+    const FwdPlan pl = plan_fwd(B, H, T, d, dv, chunk, dtype, sm, true, SIZE_MAX);
+    if (pl.nranges == 2 && pl.meet < 0) return pl.ws_bytes + pub_bytes((int64_t)B * H, d, dv);
+    return pl.ws_bytes;
 }
 
 int la_prefill_state(const void* q, const void* k, const void* v, void* out_last, const float* M_in,
