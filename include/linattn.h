@@ -95,7 +95,12 @@ int la_causal_fwd(const void* q, const void* k, const void* v, void* out,
  *              "Segment-Wise Attention" page) without copies.
  *   workspace  device scratch of workspace_bytes (256-byte aligned), or NULL/0.
  *              la_causal_fwd_workspace_size() gives the size that enables the
- *              sequence-split schedule; with less, the single-range schedule runs. */
+ *              sequence-split schedule; with less, the single-range schedule runs.
+ *              On long sequences (at least 256 chunks of 64 tokens) split over two
+ *              ranges per head, the first range hands its state to the second through
+ *              the workspace inside the launch, which is then a cooperative launch (all
+ *              blocks resident at once; it fits whenever that schedule is chosen). Calls
+ *              that share one workspace must not run concurrently. */
 int la_causal_fwd_ex(const void* q, const void* k, const void* v, void* out,
                      const float* M_in, const float* z_in, float* M_out, float* z_out,
                      int B, int H, int64_t T, int d, int dv, int chunk, float eps,
