@@ -421,3 +421,21 @@ def test_bf16_fused_state_hand_off(monkeypatch, d, dv, T):
         errs.append(oracle.rel_err_state(to_host(z_seg[s]), r_z[s], (2,)))
     print(f"PARITY hand_off_d{d}_dv{dv}_T{T} max={max(errs):.3e}")
     assert all(e <= TOL_BF16 for e in errs), errs
+
+
+def test_bf16_hand_off_long_ragged_segments(monkeypatch):
+    """The hand-off at its default threshold (313 chunks): a 20000-token sequence in segments of
+    2048 (the last one 1568 tokens) with an initial state, two ranges per head."""
+    monkeypatch.setenv("LA_FWD_RANGES", "2")
+    B, H, T, d, seg_len = 1, 2, 20000, 128, 2048
+    q, k, v = _inputs(760, B, H, T, d, d, "bf16", 0.5)
+    M0, z0 = rand_state(761, B, H, d, d)
+    out, M_seg, z_seg, n = _segments(to_dev(q), to_dev(k), to_dev(v), to_dev(M0), to_dev(z0), seg_len, True)
+    assert n == 1
+    r_out, r_M, r_z = _segment_refs(q, k, v, M0, z0, seg_len)
+    errs = [oracle.rel_err_rows(to_host(out), r_out)]
+    for s in range(len(r_M)):
+        errs.append(oracle.rel_err_state(to_host(M_seg[s]), r_M[s], (2, 3)))
+        errs.append(oracle.rel_err_state(to_host(z_seg[s]), r_z[s], (2,)))
+    print(f"PARITY hand_off_long_ragged max={max(errs):.3e} ({len(r_M)} segments)")
+    assert all(e <= TOL_BF16 for e in errs), errs
