@@ -84,6 +84,14 @@ __device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity, volat
     return __syncthreads_and(ok) != 0;
 }
 
+// Two bounded waits by every thread, then one block-wide barrier.
+__device__ __forceinline__ bool block_wait2(uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2,
+                                            volatile int* abort_flag, int* status) {
+    const bool ok = mbar_wait(b1, p1, abort_flag) && mbar_wait(b2, p2, abort_flag);
+    if (!ok) record_timeout(status, abort_flag);
+    return __syncthreads_and(ok) != 0;
+}
+
 __device__ __forceinline__ void sync_tc() {
     tc_fence_before();
     __syncthreads();
@@ -462,12 +470,9 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         const float* zc = zf + s * D;
         float* zn = zf + (s ^ 1) * D;
         if (tid == 0 && more) load_qk(idx + 1);
-        ok = block_wait(&bars[B_QK0 + s], (idx >> 1) & 1, abort_flag, p.status);
+        ok = block_wait2(&bars[B_QK0 + s], (idx >> 1) & 1, &bars[B_V], idx & 1, abort_flag, p.status);
         if (!ok) break;
-        ++pend[B_QK0 + s].waited;
-        ok = block_wait(&bars[B_V], idx & 1, abort_flag, p.status);
-        if (!ok) break;
-        ++pend[B_V].waited;
+        ++pend[B_QK0 + s].waited, ++pend[B_V].waited;
         tc_fence_after();
         const uint64_t dQk = sdesc_sw128(smem_u32(qt), 16, 1024);     // phi(Q), K-major (K = d)
         const uint64_t dQm = sdesc_sw128(smem_u32(qt), ATOM, 1024);   // phi(Q), MN-major (M = d, K = tokens)
@@ -494,12 +499,9 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
             for (int w = 0; w < 4; ++w) a += zpart[w * D + act];
             zn[act] = a;
         }
-        ok = block_wait(&bars[B_MMA], mph & 1, abort_flag, p.status);
+        ok = block_wait2(&bars[B_MMA], mph & 1, &bars[B_O], idx & 1, abort_flag, p.status);
         if (!ok) break;
-        ++mph, ++pend[B_MMA].waited;
-        ok = block_wait(&bars[B_O], idx & 1, abort_flag, p.status);
-        if (!ok) break;
-        ++pend[B_O].waited;
+        ++mph, ++pend[B_MMA].waited, ++pend[B_O].waited;
         tc_fence_after();
         // ---- P pass: P (f32), D_t, G = dout / D (high and low parts)
         if (tok) {
@@ -857,12 +859,9 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         if (tid == 0 && more) load_qk(idx + 1);
         float nd = 1.f, ne = 0.f;  // the next chunk's D_t and e_t (aux warps 6-7), stored at the end
         if (!tok && act >= 64 && more) load_de(idx + 1, nd, ne);
-        ok = block_wait(&bars[B_QK0 + s], (idx >> 1) & 1, abort_flag, p.status);
+        ok = block_wait2(&bars[B_QK0 + s], (idx >> 1) & 1, &bars[B_O], idx & 1, abort_flag, p.status);
         if (!ok) break;
-        ++pend[B_QK0 + s].waited;
-        ok = block_wait(&bars[B_O], idx & 1, abort_flag, p.status);
-        if (!ok) break;
-        ++pend[B_O].waited;
+        ++pend[B_QK0 + s].waited, ++pend[B_O].waited;
         // ---- G = dout / D: high parts into [G; R], low parts; every warp (no TMEM access):
         // thread tid takes query row tid % 64 and a quarter of the DV columns
         if (!tok && act < D) rn[act] = rc[act];  // r before this chunk, completed during g2
@@ -882,7 +881,7 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
             }
             fence_proxy_async_smem();
         }
-        sync_tc();
+        tc_fence_before();  // (the barrier of the V wait orders the G tiles before g1)
         ok = block_wait(&bars[B_V], idx & 1, abort_flag, p.status);
         if (!ok) break;
         ++pend[B_V].waited;
