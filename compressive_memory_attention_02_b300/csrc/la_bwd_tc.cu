@@ -469,10 +469,12 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         uint8_t* kt = ktile(idx);
         const float* zc = zf + s * D;
         float* zn = zf + (s ^ 1) * D;
-        if (tid == 0 && more) load_qk(idx + 1);
+        // (this barrier also ends the previous chunk: its end phase has read the stage that the
+        // next prefetch overwrites, and z before this chunk)
         ok = block_wait2(&bars[B_QK0 + s], (idx >> 1) & 1, &bars[B_V], idx & 1, abort_flag, p.status);
         if (!ok) break;
         ++pend[B_QK0 + s].waited, ++pend[B_V].waited;
+        if (tid == 0 && more) load_qk(idx + 1);
         tc_fence_after();
         const uint64_t dQk = sdesc_sw128(smem_u32(qt), 16, 1024);     // phi(Q), K-major (K = d)
         const uint64_t dQm = sdesc_sw128(smem_u32(qt), ATOM, 1024);   // phi(Q), MN-major (M = d, K = tokens)
@@ -667,7 +669,7 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
                 p.E[(int64_t)bh * p.T + t0 + t] = e;
             }
         }
-        sync_tc();
+        tc_fence_before();  // (the next chunk's first wait is the barrier)
     }
     if (ok && n > 0) {
         // the range's share of the state gradient: sum phi(Q)^T G (TMEM) and sum phi(Q)^T e
@@ -856,12 +858,13 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         const float* ec = evs + s * 64;
         const float* rc = rv + s * D;
         float* rn = rv + (s ^ 1) * D;
-        if (tid == 0 && more) load_qk(idx + 1);
         float nd = 1.f, ne = 0.f;  // the next chunk's D_t and e_t (aux warps 6-7), stored at the end
         if (!tok && act >= 64 && more) load_de(idx + 1, nd, ne);
+        // (this barrier also ends the previous chunk: its stage is read and R's tile written)
         ok = block_wait2(&bars[B_QK0 + s], (idx >> 1) & 1, &bars[B_O], idx & 1, abort_flag, p.status);
         if (!ok) break;
         ++pend[B_QK0 + s].waited, ++pend[B_O].waited;
+        if (tid == 0 && more) load_qk(idx + 1);
         // ---- G = dout / D: high parts into [G; R], low parts; every warp (no TMEM access):
         // thread tid takes query row tid % 64 and a quarter of the DV columns
         if (!tok && act < D) rn[act] = rc[act];  // r before this chunk, completed during g2
@@ -1019,7 +1022,7 @@ __global__ void __launch_bounds__(BT, D == 64 && DV == 64 ? 2 : 1)
         }
         state_to_tile_split<D, DV>(tmem + L::TRR, sm + L::GR + ATOM, L::GRB, warp, lane);
         fence_proxy_async_smem();
-        sync_tc();
+        tc_fence_before();  // (the next chunk's first wait is the barrier)
     }
     if (ok && r == 0 && n > 0 && !p.scanned) {
         // range 0 has added every chunk's share: (R, r) is now the gradient of the initial state
