@@ -609,8 +609,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         bool ok = true;
         for (int m = 0; m < n_main; ++m) {
             const int buf = m & 1;
+            // (with z in lanes 64-127 the E warps form 1/den themselves and read nothing the S
+            // warps write, and PV_m's commit already follows P_m. Nor do the S warps wait for E
+            // there, so P_{m+2} may complete p_full[buf]'s next phase before E looks at it: E
+            // does not wait on p_full at all then.)
             ok = bar_and(3, 256, mbar_wait(&o_full[buf], (m >> 1) & 1, abort_flag) &&
-                                     mbar_wait(&p_full[buf], (m >> 1) & 1, abort_flag));
+                                     (L::ZL || mbar_wait(&p_full[buf], (m >> 1) & 1, abort_flag)));
             if (!ok) break;
             tc_fence_after();
             if (L::ZL && q == 2) {
