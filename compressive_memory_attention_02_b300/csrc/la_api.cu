@@ -104,13 +104,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 4-D bf16 map {inner, T, H, B} over a strided [B, H, T, inner] tensor; 64 x 64 boxes,
 // 128-byte swizzle (the operand layout the kernels' descriptors assume), zero fill.
+// Tiled map of a [B][H][T][inner] bf16 tensor (element strides st, sh, sb): boxes of 64
+// features x `rows` tokens, 128-byte swizzle
 static bool make_map(CUtensorMap* m, const void* base, int inner, int64_t T, int H, int B, int64_t st, int64_t sh,
-                     int64_t sb) {
+                     int64_t sb, int rows = 64) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)T, (cuuint64_t)H, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-    cuuint32_t box[4] = {64, 64, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -357,7 +359,13 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, cons
                                                  ((sizeof(float) * (size_t)BH * rec + 255) / 256) * 256);
             fp.meet = pl.meet;
         }
-        rc = cuda_rc(launch_fwd_tc(fp, d, dv, B, mq, mk, mv, mo, stream));
+        // at d = dv = 64 the fused schedule's state-only chunks stream two at a time (128-token boxes)
+        CUtensorMap mk2 = mk, mv2 = mv;
+        if (pl.split > 0 && d == 64 && dv == 64 &&
+            !(make_map(&mk2, k, d, T, H, B, st.k_st, st.k_sh, st.k_sb, 128) &&
+                              make_map(&mv2, v, dv, T, H, B, st.v_st, st.v_sh, st.v_sb, 128)))
+            return LA_ERR_CUDA;
+        rc = cuda_rc(launch_fwd_tc(fp, d, dv, B, mq, mk, mv, mo, mk2, mv2, stream));
         if (!rc) ++t_launches;
         return rc;
     }

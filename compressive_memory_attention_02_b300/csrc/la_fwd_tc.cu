@@ -48,7 +48,10 @@
 //
 // Sequence split: in the fused two-range schedule (split > 0) range 1 first forms
 // the state of chunks [0, split) itself (phi(K) and the update only) while range 0
-// runs its main pass over the same chunks. With a hand-off area (pub), range 0 writes its
+// runs its main pass over the same chunks. Those state-only chunks go through the ring at
+// d = 128; at d = dv = 64 they stream two chunks per stage (one 128-row box per tensor, two
+// stages over the ring's Q and K slots): a copy engine moves a 128-row box in little more
+// time than a 64-row one, and at that width the boxes, not the bytes, set a stage's pace. With a hand-off area (pub), range 0 writes its
 // state after chunk `meet` to it and range 1 forms only the sum of chunks meet+1 .. split-1,
 // then adds the published state (a word per head: armed by range 1 at its start, set by
 // range 0 once the state is written, cleared by range 1 after reading it; every wait on it
@@ -78,6 +81,17 @@ struct FwdLayout {
     // issues them two chunks ahead; a 5-stage ring keeps their operands landed in time
     static constexpr bool AHEAD = D == 64 && DV == 64;
     static constexpr int NST = AHEAD ? 5 : 3;
+    // d = dv = 64: state-only chunks (range 1 of the fused schedule) stream in stages of two
+    // chunks, one 128-row box per tensor, since an SM's copy engine takes almost as long for a
+    // 64-row box as for a 128-row one. Two such stages lie over the ring's Q and K slots (below
+    // its ones atoms), which the main chunks take over once their products are done. (At
+    // d = 128 two 64 KB stages are too few for the load, phi and update round trip: there the
+    // state-only chunks go through the ring itself, 64 rows at a time.)
+    static constexpr bool AGG2 = AHEAD;
+    static constexpr int AGGR = 2 * CH;
+    static constexpr int AKB = D / 64 * AGGR * 128;
+    static constexpr int AVB = DV / 64 * AGGR * 128;
+    static constexpr int AST = AKB + AVB;
     static constexpr int QB = D / 64 * ATOM;
     static constexpr int KB = D / 64 * ATOMK;
     static constexpr int VB = (ZL ? 2 : DV / 64) * ATOM;
@@ -89,7 +103,7 @@ struct FwdLayout {
     static constexpr int ONES = OT + DV / 64 * ATOM;  // 16 x 64 bf16 ones (2 KB, 1024-aligned)
     static constexpr int RDEN = ONES + 2048;          // 2 x 64 floats
     static constexpr int BAR = RDEN + 2 * 64 * 4;
-    static constexpr int NBAR = 3 * NST + 14;
+    static constexpr int NBAR = 3 * NST + 20;
     static constexpr int MISC = BAR + 8 * NBAR;
     static constexpr int TOTAL = MISC + 16;
     static constexpr int ALLOC = TOTAL + 1024;
@@ -141,7 +155,8 @@ __device__ __forceinline__ void pack16_bf16(const uint32_t* x, uint32_t* a) {
 template <int D, int DV, bool SEG, bool PUB>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, FwdTcParams p) {
+                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+                  const __grid_constant__ CUtensorMap mk2, const __grid_constant__ CUtensorMap mv2, FwdTcParams p) {
     using L = FwdLayout<D, DV>;
     constexpr int NST = L::NST;
     extern __shared__ uint8_t smem_raw[];
@@ -160,6 +175,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     uint64_t* mt_ready = s_full + 11;      // bf16 M^T written and TMEM M read (R)
     uint64_t* drain = s_full + 12;         // all MMAs finished (MMA thread only)
     uint64_t* zrow_ready = s_full + 13;    // z before the next main chunk in its K tile's row 64 (E, then R)
+    uint64_t* afull = s_full + 14;         // [2] state-only stage landed (TMA)
+    uint64_t* aempty = afull + 2;          // [2] state-only stage free (MMA commit)
+    uint64_t* aphib = afull + 4;           // [2] phi applied to its keys (F)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
 
@@ -183,7 +201,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         nws = r;
     }
     const int n_main = main_end - main_begin;
-    const int nchunks = n_agg + n_main;            // chunks streamed through the ring
+    const int n_ast = L::AGG2 ? (n_agg + 1) / 2 : 0;  // state-only stages of two chunks
+    const int n_ring_agg = L::AGG2 ? 0 : n_agg;       // state-only chunks through the ring
+    const int nchunks = n_ring_agg + n_main;          // chunks streamed through the ring
+    static_assert(!L::AGG2 || 2 * L::AST <= L::V0, "state-only stages over the ring's Q and K slots");
     const bool writes_state = (r == p.nranges - 1);
     const float* agg = p.ws ? p.ws + (int64_t)bh * (p.nranges - 1) * p.rec : nullptr;
 
@@ -195,6 +216,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         tma_prefetch_desc(&mk);
         tma_prefetch_desc(&mv);
         tma_prefetch_desc(&mo);
+        if (n_agg > 0) {
+            tma_prefetch_desc(&mk2);
+            tma_prefetch_desc(&mv2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, 512);
@@ -227,15 +252,44 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         // ======================================================== TMA producer
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();  // q, k, v are read once
+            // state-only stages: keys and values of chunks agg_begin + 2a and + 2a + 1 (when n_agg
+            // is odd the last stage's second chunk, chunk split, is loaded and not used)
+            int issued_a = 0;
+            for (int a = 0; a < n_ast; ++a) {
+                const int s = a & 1;
+                if (a >= 2 && !mbar_wait(&aempty[s], ((a >> 1) - 1) & 1, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    break;
+                }
+                const int t = (agg_begin + 2 * a) * CH;
+                uint8_t* st = sm + L::Q0 + s * L::AST;
+                mbar_expect_tx(&afull[s], (D + DV) * L::AGGR * 2);
+#pragma unroll
+                for (int a2 = 0; a2 < D / 64; ++a2)
+                    tma_load_4d_hint(st + a2 * L::AGGR * 128, &mk2, &afull[s], a2 * 64, t, h, b, pol);
+#pragma unroll
+                for (int a2 = 0; a2 < DV / 64; ++a2)
+                    tma_load_4d_hint(st + L::AKB + a2 * L::AGGR * 128, &mv2, &afull[s], a2 * 64, t, h, b, pol);
+                ++issued_a;
+            }
+            // the ring lies over those stages: their products must be done before it is loaded
+            bool ok_a = issued_a == n_ast;
+            for (int a = max(0, issued_a - 2); a < issued_a; ++a) {
+                if (ok_a && !mbar_wait(&aempty[a & 1], (a >> 1) & 1, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    ok_a = false;
+                }
+                if (!ok_a) mbar_wait_drain(&afull[a & 1], (a >> 1) & 1);
+            }
             int issued = 0;
-            for (int g = 0; g < nchunks; ++g) {
+            for (int g = 0; ok_a && g < nchunks; ++g) {
                 const int s = g % NST;
                 if (g >= NST && !mbar_wait(&empty[s], ((g / NST) - 1) & 1, abort_flag)) {
                     record_timeout(p.status, abort_flag);
                     break;
                 }
-                const bool is_main = g >= n_agg;
-                const int t = (is_main ? main_begin + g - n_agg : agg_begin + g) * CH;
+                const bool is_main = g >= n_ring_agg;
+                const int t = (is_main ? main_begin + g - n_ring_agg : agg_begin + g) * CH;
                 mbar_expect_tx(&full[s], ((is_main ? D : 0) + D + DV) * CH * 2);
 #pragma unroll
                 for (int a = 0; a < D / 64; ++a) {
@@ -268,6 +322,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             const uint64_t dp0 = sdesc_sw128(smem_u32(sm + L::PT), 16, 1024);     // P, K-major
             const uint64_t d1 = sdesc_sw128(smem_u32(sm + L::ONES), 16, 1024);    // ones, K-major
             auto off = [](uint32_t bytes) { return (uint64_t)(bytes >> 4); };
+            const uint32_t ones0 = smem_u32(sm + L::V0 + ATOM);  // the ring's first ones atom (dv = 64)
             bool ok = true;
             int mt_waits = 0;
             auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -288,9 +343,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                         mma_bf16_ss(tmem + TM_Z, kb + off(ks * 2048), d1 + off(ks * 32), id_z, 1);
                 }
             };
+            // the update over nk 16-token steps of state-only stage s: the 64-feature blocks of
+            // V^T and phi(K) lie AGGR rows apart; at dv = 64 the second block of V^T is the ring's
+            // first ones atom (64 rows of ones, read again for the stage's second chunk)
+            auto update_agg = [&](int s, int nk) {
+                const uint32_t ka = smem_u32(sm + L::Q0 + s * L::AST), va = ka + L::AKB;
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint32_t vrow = va + kk * 2048, krow = ka + kk * 2048;
+                    const uint64_t vd = sdesc_sw128(vrow, L::ZL ? ones0 + (kk & 3) * 2048 - vrow : L::AGGR * 128, 1024);
+                    const uint64_t kd = sdesc_sw128(krow, L::AGGR * 128, 1024);
+                    mma_bf16_ss(tmem + TM_M, vd, kd, id_u, 1);
+                    if constexpr (!L::ZL) mma_bf16_ss(tmem + TM_Z, kd, d1 + off((kk & 3) * 32), id_z, 1);
+                }
+            };
             // S'_m of main chunk m
             auto scores = [&](int m) {
-                const int g = n_agg + m, s = g % NST, buf = m & 1;
+                const int g = n_ring_agg + m, s = g % NST, buf = m & 1;
                 const uint64_t qd = dq0 + off(s * L::QB), kd = dk0 + off(s * L::KB);
                 if (!wait(&phib[s], (g / NST) & 1)) return false;
                 if (m >= 2 && !wait(&s_free[buf], ((m >> 1) - 1) & 1)) return false;
@@ -305,7 +373,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             };
             // inter_m and update_m of main chunk m
             auto state_part = [&](int m) {
-                const int g = n_agg + m, s = g % NST, buf = m & 1;
+                const int g = n_ring_agg + m, s = g % NST, buf = m & 1;
                 const uint64_t qd = dq0 + off(s * L::QB);
                 if (!wait(mt_ready, mt_waits++ & 1)) return false;
                 if (m >= 2 && !wait(&o_free[buf], ((m >> 1) - 1) & 1)) return false;
@@ -322,7 +390,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             if (n_agg > 0) {
                 wait(mt_ready, mt_waits++ & 1);  // initial state in TMEM
                 tc_fence_after();
-                for (int g = 0; ok && g < n_agg; ++g) {
+                for (int a = 0; ok && a < n_ast; ++a) {
+                    const int s = a & 1;
+                    if (!wait(&aphib[s], (a >> 1) & 1)) break;
+                    tc_fence_after();
+                    update_agg(s, min(2, n_agg - 2 * a) * (CH / 16));
+                    mma_commit(&aempty[s]);
+                }
+                for (int g = 0; ok && g < n_ring_agg; ++g) {
                     const int s = g % NST;
                     if (!wait(&phib[s], (g / NST) & 1)) break;
                     tc_fence_after();
@@ -337,7 +412,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 if (ok && n_main > 0) front(0);
             }
             for (int m = 0; ok && m < n_main; ++m) {
-                const int g = n_agg + m, s = g % NST, buf = m & 1;
+                const int g = n_ring_agg + m, s = g % NST, buf = m & 1;
                 if (!wait(&p_full[buf], (m >> 1) & 1)) break;
                 tc_fence_after();
 #pragma unroll
@@ -505,7 +580,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
                 if (has_z) {
                     const uint32_t zb = tmem_ld1(tmem + TM_Z + lane_base);
                     tmem_wait_ld();
-                    put_zrow(sm + L::K0 + ((n_agg + mnext) % NST) * L::KB, j, __uint_as_float(zb));
+                    put_zrow(sm + L::K0 + ((n_ring_agg + mnext) % NST) * L::KB, j, __uint_as_float(zb));
                     fence_proxy_async_smem();
                 }
                 named_bar_sync(4, 128);
@@ -743,17 +818,32 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         // ======================================================== F: phi (warps 2, 3, 18-30 but 21, 25, 29)
         const int fi = warp < 4 ? warp - 2 : 2 + (warp - 18) - (warp - 17) / 4;
         const int ct = fi * 32 + lane;
-        for (int idx = ct; idx < NST * (D / 64) * 15 * 8; idx += 32 * NFW) {
-            const int c16 = idx % 8, row = 65 + (idx / 8) % 15, sa = idx / (8 * 15);
-            *reinterpret_cast<uint4*>(sm + L::K0 + sa * ATOMK + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+        // rows 65-79 of the K atoms feed only columns of S' that are never read; they are zeroed
+        // unless the state-only stages of two chunks lie over them
+        if (n_ast == 0) {
+            for (int idx = ct; idx < NST * (D / 64) * 15 * 8; idx += 32 * NFW) {
+                const int c16 = idx % 8, row = 65 + (idx / 8) % 15, sa = idx / (8 * 15);
+                *reinterpret_cast<uint4*>(sm + L::K0 + sa * ATOMK + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+            }
         }
         bool ok = true;
-        for (int g = 0; g < nchunks; ++g) {
+        for (int a = 0; a < n_ast; ++a) {  // state-only stages of two chunks: phi on their keys (full chunks)
+            const int s = a & 1;
+            ok = bar_and(1, 32 * NFW, mbar_wait(&afull[s], (a >> 1) & 1, abort_flag));
+            if (!ok) break;
+            uint8_t* kt = sm + L::Q0 + s * L::AST;
+            phi_tile<D, 32 * NFW>(kt, L::AGGR * 128, CH, ct, nullptr, p.phi_ident);
+            if (2 * a + 1 < n_agg) phi_tile<D, 32 * NFW>(kt + CH * 128, L::AGGR * 128, CH, ct, nullptr, p.phi_ident);
+            fence_proxy_async_smem();
+            named_bar_sync(1, 32 * NFW);
+            if (ct == 0) mbar_arrive(&aphib[s]);
+        }
+        for (int g = 0; ok && g < nchunks; ++g) {
             const int s = g % NST;
-            const bool is_main = g >= n_agg;
+            const bool is_main = g >= n_ring_agg;
             ok = bar_and(1, 32 * NFW, mbar_wait(&full[s], (g / NST) & 1, abort_flag));
             if (!ok) break;
-            const int64_t t0 = (int64_t)(is_main ? main_begin + g - n_agg : agg_begin + g) * CH;
+            const int64_t t0 = (int64_t)(is_main ? main_begin + g - n_ring_agg : agg_begin + g) * CH;
             const int valid = (int)min64(CH, p.T - t0);
             if (is_main) phi_tile<D, 32 * NFW>(sm + L::Q0 + s * L::QB, ATOM, CH, ct, nullptr, p.phi_ident);
             phi_tile<D, 32 * NFW>(sm + L::K0 + s * L::KB, ATOMK, valid, ct, nullptr, p.phi_ident);
@@ -774,7 +864,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
 template <int D, int DV, bool SEG, bool PUB>
 static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
+                            const CUtensorMap& mv, const CUtensorMap& mo, const CUtensorMap& mk2,
+                            const CUtensorMap& mv2, cudaStream_t s) {
     using L = FwdLayout<D, DV>;
     static_assert(L::ALLOC <= 227 * 1024, "shared memory budget");
     auto fn = fwd_tc_kernel<D, DV, SEG, PUB>;
@@ -793,21 +884,22 @@ static cudaError_t launch_t(const FwdTcParams& p, int B, const CUtensorMap& mq, 
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = PUB ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, fn, mq, mk, mv, mo, p);
+    return cudaLaunchKernelEx(&cfg, fn, mq, mk, mv, mo, mk2, mv2, p);
 }
 
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
-                          const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
+                          const CUtensorMap& mv, const CUtensorMap& mo, const CUtensorMap& mk2, const CUtensorMap& mv2,
+                          cudaStream_t s) {
     const bool seg = p.M_seg || p.z_seg;
     const bool pub = p.pub != nullptr && p.split > 0;
     if (seg && p.seg_chunks <= 0) return cudaErrorInvalidValue;
     if (pub && (!p.pub_flag || p.meet < 0 || p.meet > p.split - 2)) return cudaErrorInvalidValue;
 #define LA_FWD_SHAPE(DD, DDV)                                                                         \
     if (d == DD && dv == DDV) {                                                                       \
-        if (seg) return pub ? launch_t<DD, DDV, true, true>(p, B, mq, mk, mv, mo, s)                  \
-                            : launch_t<DD, DDV, true, false>(p, B, mq, mk, mv, mo, s);                \
-        return pub ? launch_t<DD, DDV, false, true>(p, B, mq, mk, mv, mo, s)                          \
-                   : launch_t<DD, DDV, false, false>(p, B, mq, mk, mv, mo, s);                        \
+        if (seg) return pub ? launch_t<DD, DDV, true, true>(p, B, mq, mk, mv, mo, mk2, mv2, s)                  \
+                            : launch_t<DD, DDV, true, false>(p, B, mq, mk, mv, mo, mk2, mv2, s);                \
+        return pub ? launch_t<DD, DDV, false, true>(p, B, mq, mk, mv, mo, mk2, mv2, s)                          \
+                   : launch_t<DD, DDV, false, false>(p, B, mq, mk, mv, mo, mk2, mv2, s);                        \
     }
     LA_FWD_SHAPE(128, 128)
     LA_FWD_SHAPE(128, 64)

@@ -177,7 +177,8 @@ cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 // with 64 x 64 boxes and 128-byte swizzle.
 cudaError_t launch_parts_tc(const PartsParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdTcParams& p, int d, int dv, int B, const CUtensorMap& mq, const CUtensorMap& mk,
-                          const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s);
+                          const CUtensorMap& mv, const CUtensorMap& mo, const CUtensorMap& mk2, const CUtensorMap& mv2,
+                          cudaStream_t s);
 
 // Positive random-feature map (la_fmap.cu): maps {d, rows} over x [rows, d] and {d, m} over
 // W [m, d], both bf16; out [rows, m] bf16.
